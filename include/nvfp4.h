@@ -1,0 +1,185 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 / MXFP4 block-scaled GEMM library.
+ *
+ * Operations (each entry point cites the passage that defines it):
+ *   nvfp4_quantize      bf16 -> NVFP4 (packed e2m1 + e4m3 scale per 16, 128x4 swizzled scales)
+ *   nvfp4_gemm          D[M,N] = alpha * deq(A) deq(B)^T, bf16 out, fp32 accumulation
+ *   mxfp4_quantize      bf16 -> MXFP4 (packed e2m1 + ue8m0 scale per 32), optionally grouped by expert
+ *   mxfp4_grouped_gemm  per-expert D_e = alpha * deq(A_e) deq(B_e)^T for MoE experts
+ *   sf_swizzle          row-major scale matrix <-> 128x4 swizzled layout
+ *
+ * Sources ("page, section"):
+ *   [vLLM-SM103]  vLLM fork compare view "add pdl" (sm103 branch)
+ *   [FI-4865]     FlashInfer PR 4865 "perf(gemm): optimize SM103 CuTe DSL mm_fp4 kernel"
+ *   [FI-4466]     FlashInfer PR 4466 "sm100 cute_dsl w4a16 gemm" (follow-up PR 4620 text)
+ *   [vLLM-51158]  vLLM PR 51158 "Enable CUTLASS MXFP4 W4A4 MoE on SM12x"
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *     allocates device memory and keeps no pointer after the call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Arguments are validated on the host before anything is enqueued.  On error nothing
+ *     is launched, the status is returned and nvfp4_last_error() describes it.
+ *   - Sizes of zero rows are legal and enqueue nothing.
+ *   - The current device must be compute capability 10.3 (sm_103).
+ *   - Packed FP4: element 2t of a row is the low nibble of byte t, element 2t+1 the high one.
+ *   - 128x4 scale layout: a scale matrix of R rows and C scale columns is stored as
+ *     round_up(R,128) * round_up(C,4) bytes; scale (r, j) sits at byte
+ *       ((r/128) * (round_up(C,4)/4) + j/4) * 512 + (r%32)*16 + ((r/32)%4)*4 + j%4
+ *     ([vLLM-SM103] nvfp4_quant_kernels.cu "Scale factor layout conversion: SM100 <-> SM103",
+ *     SM100 offset; nvfp4_utils.cuh tile base).  Padding bytes must hold 0x00 (the
+ *     quantisers write them so).
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad enum value */
+  NVFP4_ERR_MISALIGNED = 2,         /* pointer or stride alignment rule broken */
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 3,  /* divisibility rule broken (K % 32, N % 32, ...) */
+  NVFP4_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103 */
+  NVFP4_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed (message has the name) */
+  NVFP4_ERR_TIMEOUT = 6             /* a kernel gave up a bounded wait (nvfp4_check_status) */
+} nvfp4_status_t;
+
+/* Launch flags (bitwise OR). */
+enum {
+  /* Launch with programmatic dependent launch (cudaLaunchAttributeProgrammaticStreamSerialization):
+   * the kernel may start while the previous kernel on the stream is still running.  Every
+   * kernel of this library waits (griddepcontrol.wait) before it reads an input that a
+   * predecessor may produce or writes any output, and signals its own dependents
+   * (griddepcontrol.launch_dependents) once its input reads are issued.  Exception, stated
+   * per entry point: nvfp4_gemm and mxfp4_grouped_gemm may read the weight operand B and its
+   * scales before the wait, so B must not be written by the kernels it overlaps.
+   * [vLLM-SM103] summary.md "What is PDL?", nvfp4_quant_kernels.cu "Host entry: SM103
+   * activation quantization" (use_pdl). */
+  NVFP4_FLAG_PDL = 1u << 0,
+  /* Short (about 20 ms) limit on every pipeline wait instead of the default (about 10 s);
+   * for tests of the timeout path. */
+  NVFP4_FLAG_DEBUG_TIMEOUT = 1u << 8
+};
+
+/* Message for the last error on the calling thread ("" when the last call succeeded). */
+const char *nvfp4_last_error(void);
+
+/* Bytes of a swizzled scale buffer for `rows` rows of `k` elements with one scale per
+ * `sf_vec` (16 for NVFP4, 32 for MXFP4): round_up(rows,128) * round_up(k/sf_vec, 4).
+ * Returns 0 for invalid arguments.  Host only. */
+size_t nvfp4_sf_bytes(int64_t rows, int64_t k, int sf_vec);
+
+/* Bytes of the grouped MXFP4 scale buffer that mxfp4_quantize writes for `total_rows` rows
+ * split over `num_experts` experts: an upper bound of sum_e round_up(M_e,128) rows, namely
+ * (round_up(total_rows,128) + 128*num_experts) * round_up(k/32,4).  Host only. */
+size_t mxfp4_grouped_sf_bytes(int64_t total_rows, int num_experts, int64_t k);
+
+/* NVFP4 activation quantisation.
+ * Source: [vLLM-SM103] nvfp4_quant_kernels.cu "SM103 (B300) activation quantization kernel"
+ * (one fp32 global scale, a scale per 16 elements of a row, packed e2m1 out, swizzled scales,
+ * padded scale rows/columns quantised from zero input) and test_nvfp4_quant.py (global scale
+ * = 448*6/amax).  Per 16-element block, in fp32 with round-to-nearest-even on every step:
+ *   s = (gs*amax)/6; sc = e4m3_satfinite(s); inv = sd ? gs/sd : 0 (sd = value of sc);
+ *   q_i = e2m1_satfinite(x_i * inv) (the sign of a zero result is kept).
+ *   x        bf16 [m, k], row stride `ldx` elements (ldx >= k, ldx % 8 == 0), 16-B aligned
+ *   gs       device fp32 scalar (global scale), 4-B aligned
+ *   q        uint8 [m, k/2] row-major, 8-B aligned
+ *   sf       uint8 [nvfp4_sf_bytes(m, k, 16)], 16-B aligned; every byte is written
+ *   k % 16 == 0.  Reads x/gs and writes q/sf only after the PDL wait. */
+nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, int64_t ldx, const float *gs,
+                              uint8_t *q, uint8_t *sf, uint32_t flags, nvfp4_stream_t stream);
+
+/* MXFP4 quantisation ("e2m1 data with e8m0 scale per 32", [vLLM-51158] "Changes",
+ * mxfp4_experts_quant.cu).  Per 32-element block: s = amax/6 (fp32); scale = smallest power
+ * of two >= s (ue8m0 code clamped to [0,254], 0 for an all-zero block);
+ * q_i = e2m1_satfinite(x_i * 2^(127-code)).
+ *   x            bf16 [t, k], row stride ldx (ldx >= k, ldx % 8 == 0), 16-B aligned
+ *   row_offsets  NULL for one dense scale block of round_up(t,128) rows; otherwise a DEVICE
+ *                int64 [num_experts+1] array, non-decreasing, row_offsets[0] == 0,
+ *                row_offsets[num_experts] == t: rows of expert e are row_offsets[e] ..
+ *                row_offsets[e+1]-1 and their scales form their own zero-padded 128-row
+ *                block starting at scale row sum_{j<e} round_up(M_j,128).
+ *   q            uint8 [t, k/2]; sf uint8 [sf_bytes] (16-B aligned), sf_bytes >=
+ *                nvfp4_sf_bytes(t,k,32) (dense) or mxfp4_grouped_sf_bytes(t,E,k) (grouped).
+ *   k % 32 == 0, 1 <= num_experts <= 1024 when row_offsets != NULL.
+ *   Offsets that break the rules above are a caller error; the kernel never writes outside
+ *   q[0..t) rows or sf[0..sf_bytes). */
+nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, int64_t ldx,
+                              const int64_t *row_offsets, int num_experts, uint8_t *q, uint8_t *sf,
+                              size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream);
+
+/* The tile configuration nvfp4_gemm picks for a shape (M-based selector, [vLLM-SM103]
+ * nvfp4_scaled_mm_kernels.cu "SM103 Dispatch"; narrow tiles for small M, [FI-4865]
+ * "Reviewer Notes").  Host only. */
+typedef struct {
+  int swap_ab;   /* 1: the weight B fills the 128-row MMA slot and tokens the N slot */
+  int tile_m;    /* rows of the MMA tile (128) */
+  int tile_n;    /* MMA N */
+  int splits;    /* K splits reduced inside a thread-block cluster (1 = none) */
+  int stages;    /* shared-memory pipeline depth */
+  int ctas;      /* CTAs launched */
+} nvfp4_gemm_plan_t;
+nvfp4_status_t nvfp4_gemm_plan(int64_t m, int64_t n, int64_t k, nvfp4_gemm_plan_t *plan);
+
+/* NVFP4 block-scaled GEMM with bf16 output.
+ * Source: [vLLM-SM103] nvfp4_scaled_mm_kernels.cu "SM103 Entry Point" (A [M,K/2] packed e2m1
+ * row-major, B [N,K/2] packed e2m1 K-major, scale_a/scale_b e4m3 in the 128x4 layout padded to
+ * [round_up(rows,128), round_up(K/16,4)], alpha fp32 [1], k % 32 == 0, n % 32 == 0);
+ * [FI-4865] "2. Alpha epilogue bug" (alpha multiplies the fp32 accumulator, then ONE
+ * conversion to bf16) and "3. Restore 256-bit stores" (D compact N-major, 32-B aligned).
+ *   D[m,n] = bf16( alpha * sum_k e2m1(A[m,k]) e4m3(sfa[m,k/16]) e2m1(B[n,k]) e4m3(sfb[n,k/16]) )
+ *   a      uint8 [m, k/2], 32-B aligned         sfa  nvfp4_sf_bytes(m,k,16) bytes, 16-B aligned
+ *   b      uint8 [n, k/2], 32-B aligned         sfb  nvfp4_sf_bytes(n,k,16) bytes, 16-B aligned
+ *   alpha  device fp32 scalar, 4-B aligned       d    bf16 [m, n] row-major, 32-B aligned
+ *   n % 32 == 0, k % 32 == 0, m, n, k < 2^31.
+ * With NVFP4_FLAG_PDL, b and sfb may be read before the wait for the preceding kernel. */
+nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb,
+                          const float *alpha, void *d, int64_t m, int64_t n, int64_t k,
+                          uint32_t flags, nvfp4_stream_t stream);
+
+/* MXFP4 grouped (MoE) GEMM: for every expert e, D[rows of e, :] = alpha * deq(A_e) deq(B_e)^T.
+ * Source: [vLLM-51158] "Changes" (CUTLASS MXFP4 grouped GEMM over experts; SM10x/SM12x share
+ * the block-scaled scale layout) and [vLLM-SM103] ops.h (expert offsets as arguments).
+ *   a            uint8 [t, k/2] (rows sorted by expert), 32-B aligned
+ *   sfa          grouped ue8m0 scales as mxfp4_quantize(row_offsets) writes them, 16-B aligned
+ *   row_offsets  DEVICE int64 [num_experts+1] (same rules as mxfp4_quantize)
+ *   b            uint8 [num_experts, n, k/2], 32-B aligned
+ *   sfb          uint8 [num_experts, nvfp4_sf_bytes(n,k,32)] (each expert's block swizzled)
+ *   alpha        device fp32 scalar or NULL for 1.0
+ *   d            bf16 [t, n] row-major, 32-B aligned
+ *   n % 32 == 0, k % 32 == 0, 1 <= num_experts <= 1024.
+ * With NVFP4_FLAG_PDL, b and sfb may be read before the wait for the preceding kernel. */
+nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const int64_t *row_offsets,
+                                  int num_experts, const uint8_t *b, const uint8_t *sfb,
+                                  const float *alpha, void *d, int64_t t, int64_t n, int64_t k,
+                                  uint32_t flags, nvfp4_stream_t stream);
+
+/* Scale layout conversion between a row-major scale matrix [rows, cols] (bytes) and the
+ * 128x4 swizzled layout of nvfp4_sf_bytes size (swizzle writes the zero padding).
+ * Source: [vLLM-SM103] nvfp4_utils.py swizzle_blockscale (pad to (128,4), then block
+ * interleave) and the in-tile offset quoted at the top of this header.
+ *   to_swizzled = 1: src [rows, cols] row-major -> dst swizzled
+ *   to_swizzled = 0: src swizzled -> dst [rows, cols] row-major
+ * Buffers must not overlap.  No alignment requirement. */
+nvfp4_status_t sf_swizzle(const uint8_t *src, uint8_t *dst, int64_t rows, int64_t cols,
+                          int to_swizzled, nvfp4_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status word that kernels set when a
+ * bounded pipeline wait gave up.  Returns NVFP4_ERR_TIMEOUT if any kernel timed out since the
+ * last check, NVFP4_ERR_CUDA if the synchronisation failed, NVFP4_OK otherwise. */
+nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,194 @@
+"""GB300 (sm_103a) NVFP4 / MXFP4 block-scaled GEMM library -- Python binding of libnvfp4.so.
+
+Thin ctypes marshalling over the C ABI in include/nvfp4.h: each function here has the name of
+the C entry point it calls, takes torch CUDA tensors, allocates missing outputs with
+torch.empty, and passes raw pointers and the current CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; there is no CPU fallback.  Importing fails if libnvfp4.so is missing
+(build it with ``python -m nvfp4_block_scaled_bf16_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is not built: run `python -m nvfp4_block_scaled_bf16_gb300.build`")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_i64, _u32, _int, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+
+FLAG_PDL = 1 << 0
+FLAG_DEBUG_TIMEOUT = 1 << 8
+
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_MISALIGNED",
+          3: "NVFP4_ERR_UNSUPPORTED_SHAPE", 4: "NVFP4_ERR_UNSUPPORTED_DEVICE", 5: "NVFP4_ERR_CUDA",
+          6: "NVFP4_ERR_TIMEOUT"}
+
+
+class PlanT(ctypes.Structure):
+    _fields_ = [("swap_ab", _int), ("tile_m", _int), ("tile_n", _int), ("splits", _int),
+                ("stages", _int), ("ctas", _int)]
+
+
+_SIGS = {
+    "nvfp4_last_error": (ctypes.c_char_p, []),
+    "nvfp4_sf_bytes": (_sz, [_i64, _i64, _int]),
+    "mxfp4_grouped_sf_bytes": (_sz, [_i64, _int, _i64]),
+    "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
+    "mxfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u32, _vp]),
+    "nvfp4_gemm_plan": (_int, [_i64, _i64, _i64, ctypes.POINTER(PlanT)]),
+    "nvfp4_gemm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
+    "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
+    "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
+    "nvfp4_check_status": (_int, [_vp]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+lib = _lib  # raw ctypes handle (tests call entry points through it directly)
+LIB_PATH = _LIB_PATH
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS.get(code, code)}: {message}")
+        self.code = code
+
+
+def last_error() -> str:
+    return _lib.nvfp4_last_error().decode()
+
+
+def _check(code: int) -> None:
+    if code != 0:
+        raise NVFP4Error(code, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, name, dim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions")
+
+
+def sf_bytes(rows: int, k: int, sf_vec: int = 16) -> int:
+    """Bytes of a 128x4-swizzled scale buffer: round_up(rows,128) * round_up(k/sf_vec, 4)."""
+    return int(_lib.nvfp4_sf_bytes(rows, k, sf_vec))
+
+
+def grouped_sf_bytes(total_rows: int, experts: int, k: int) -> int:
+    return int(_lib.mxfp4_grouped_sf_bytes(total_rows, experts, k))
+
+
+def nvfp4_gemm_plan(m: int, n: int, k: int) -> dict:
+    p = PlanT()
+    _check(_lib.nvfp4_gemm_plan(m, n, k, ctypes.byref(p)))
+    return {f: getattr(p, f) for f, _ in PlanT._fields_}
+
+
+def nvfp4_quantize(x, gs, q=None, sf=None, flags: int = 0, stream=None):
+    """bf16 [m, k] -> (packed e2m1 uint8 [m, k/2], swizzled e4m3 scales uint8 [sf_bytes])."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(gs, torch.float32, "gs")
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    m, k = x.shape
+    if q is None:
+        q = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(sf_bytes(m, k, 16), dtype=torch.uint8, device=x.device)
+    _check(_lib.nvfp4_quantize(_ptr(x), m, k, x.stride(0), _ptr(gs), _ptr(q), _ptr(sf), flags, _stream(stream)))
+    return q, sf
+
+
+def mxfp4_quantize(x, row_offsets=None, q=None, sf=None, flags: int = 0, stream=None):
+    """bf16 [t, k] -> (packed e2m1 [t, k/2], ue8m0 scales); grouped per expert with row_offsets [E+1]."""
+    _need(x, torch.bfloat16, "x", 2)
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    t, k = x.shape
+    experts = 0
+    if row_offsets is not None:
+        _need(row_offsets, torch.int64, "row_offsets", 1)
+        experts = row_offsets.numel() - 1
+    need = grouped_sf_bytes(t, experts, k) if row_offsets is not None else sf_bytes(t, k, 32)
+    if q is None:
+        q = torch.empty((t, k // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    _check(_lib.mxfp4_quantize(_ptr(x), t, k, x.stride(0), _ptr(row_offsets), experts, _ptr(q), _ptr(sf),
+                               sf.numel(), flags, _stream(stream)))
+    return q, sf
+
+
+def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None):
+    """D[m, n] = bf16(alpha * deq(a) @ deq(b)^T); a [m, k/2], b [n, k/2] packed uint8."""
+    _need(a, torch.uint8, "a", 2)
+    _need(b, torch.uint8, "b", 2)
+    _need(sfa, torch.uint8, "sfa")
+    _need(sfb, torch.uint8, "sfb")
+    _need(alpha, torch.float32, "alpha")
+    m, kh = a.shape
+    n = b.shape[0]
+    if b.shape[1] != kh:
+        raise ValueError("a and b disagree on K")
+    for t_, name in ((a, "a"), (b, "b")):
+        if not t_.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if sfa.numel() < sf_bytes(m, 2 * kh) or sfb.numel() < sf_bytes(n, 2 * kh):
+        raise ValueError("scale buffers are too small")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh, flags,
+                           _stream(stream)))
+    return d
+
+
+def mxfp4_grouped_gemm(a, sfa, row_offsets, b, sfb, alpha=None, d=None, flags: int = 0, stream=None):
+    """Per expert e: D[rows of e] = bf16(alpha * deq(A_e) @ deq(B_e)^T); b [E, n, k/2]."""
+    _need(a, torch.uint8, "a", 2)
+    _need(b, torch.uint8, "b", 3)
+    _need(row_offsets, torch.int64, "row_offsets", 1)
+    t, kh = a.shape
+    experts, n, kb = b.shape
+    if kb != kh or row_offsets.numel() != experts + 1:
+        raise ValueError("shape mismatch")
+    if d is None:
+        d = torch.empty((t, n), dtype=torch.bfloat16, device=a.device)
+    _check(_lib.mxfp4_grouped_gemm(_ptr(a), _ptr(sfa), _ptr(row_offsets), experts, _ptr(b), _ptr(sfb),
+                                   _ptr(alpha), _ptr(d), t, n, 2 * kh, flags, _stream(stream)))
+    return d
+
+
+def sf_swizzle(src, rows: int, cols: int, to_swizzled: bool = True, dst=None, stream=None):
+    """Row-major scale bytes [rows, cols] <-> 128x4 swizzled buffer."""
+    _need(src, torch.uint8, "src")
+    if dst is None:
+        n = (-(-rows // 128) * 128) * (-(-cols // 4) * 4) if to_swizzled else rows * cols
+        dst = torch.empty(n, dtype=torch.uint8, device=src.device)
+    _check(_lib.sf_swizzle(_ptr(src), _ptr(dst), rows, cols, 1 if to_swizzled else 0, _stream(stream)))
+    return dst
+
+
+def check_status(stream=None) -> None:
+    """Raise NVFP4Error(TIMEOUT) if a kernel gave up a bounded wait since the last check."""
+    _check(_lib.nvfp4_check_status(_stream(stream)))

@@ -1,0 +1,449 @@
+// Warp-specialised block-scaled FP4 GEMM for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes (vLLM fork compare view "add pdl", nvfp4_scaled_mm_kernels.cu, "SM103 Entry
+// Point"; FlashInfer PR 4865, "2. Alpha epilogue bug" and "3. Restore 256-bit stores"):
+//   C[i, j] = sum_k deq(A)[i, k] * deq(B)[j, k]   (fp32 accumulation in tensor memory)
+//   D       = bf16(alpha * C)                     (alpha on the fp32 value, one conversion)
+// A and B are K-major packed e2m1 (two per byte); their scales (ue4m3 per 16 for NVFP4, ue8m0
+// per 32 for MXFP4) are in the 128x4 swizzled layout, whose 512-byte tiles are exactly the
+// 32-row x 16-byte blocks one tcgen05.cp 32x128b.warpx4 moves into tensor memory.
+//
+// CTA = 6 warps:
+//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and scale chunks (bulk copies)
+//               into a STAGES-deep shared-memory ring, one mbarrier pair per stage;
+//   warp 1      allocates tensor memory; one lane copies the stage's scales to TMEM and issues
+//               4 MMAs (K = 64 each) per 256-wide K stage, then commits the stage back to the
+//               producer and, after the last K stage of a tile, the accumulator to the epilogue;
+//   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, alpha * acc in fp32, one RNE
+//               conversion to bf16, 256-bit stores.
+// NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
+// Tiles are walked persistently (grid <= SM count).  With splits > 1, the CTAs of a
+// (splits, 1, 1) cluster each take a slice of K for the same tile and reduce their fp32 partial
+// tiles through distributed shared memory in a fixed order, so the result is deterministic.
+//
+// Every mbarrier wait is bounded (WaitCtl).  When one gives up, the CTA records the time-out
+// in the device status word, every role leaves its loop, outstanding copies and MMAs are
+// drained with bounded waits, and tensor memory is freed before the CTA exits.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+template <int BN_, int STAGES_, bool MX_>
+struct GemmCfg {
+  static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
+  static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
+  static constexpr bool MX = MX_;         // true: MXFP4 (ue8m0 / 32); false: NVFP4 (ue4m3 / 16)
+  static constexpr int BM = 128;          // MMA M: rows of operand A per tile
+  static constexpr int KSTAGE = 256;      // K elements per stage = one 128-byte TMA row
+  static constexpr int VEC = MX ? 32 : 16;
+  static constexpr int CHUNKS = KSTAGE / VEC / 4;  // 512-byte scale chunks per 128 rows per stage
+  static constexpr int SFB_BLOCKS = (BN + 127) / 128;
+  static constexpr int A_BYTES = BM * 128;
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int SFA_BYTES = CHUNKS * 512;
+  static constexpr int SFB_BYTES = SFB_BLOCKS * CHUNKS * 512;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int SFA_COLS = CHUNKS * 4;
+  static constexpr int SFB_COLS = SFB_BLOCKS * CHUNKS * 4;
+  static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // two slots, alternating per K stage
+  static constexpr int NACC = (2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
+  static constexpr int SF_COL0 = NACC * BN;
+  static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int RED_BYTES = BM * BN * 4;  // split-K partial tile (reuses the stage ring)
+  static constexpr int MAX_EXPERTS = 1024;
+  static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
+  static constexpr int CTRL_BYTES = 256;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTRL_BYTES + TABLE_BYTES;
+  static constexpr uint32_t IDESC = idesc_block_scaled(BM, BN, MX, 0);
+  static_assert(TMEM_USED <= 512, "tensor memory budget");
+  static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(STAGE_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
+};
+
+struct GemmArgs {
+  const uint8_t *sfa;       // scales of operand A (swizzled, 128-row blocks)
+  const uint8_t *sfb;       // scales of operand B
+  const float *alpha;       // device scalar, or nullptr for 1
+  __nv_bfloat16 *d;         // output
+  int64_t ldd;              // output row stride (elements)
+  int m, n, k;              // operand A rows, operand B rows (per expert when grouped), K
+  int swap;                 // 1: D[j][i] = C[i][j] (operand A is the weight)
+  int m_tiles, n_tiles, k_tiles, splits;
+  int sf_chunks;            // 512-byte scale chunks per 128-row block = round_up(K/VEC, 4) / 4
+  const int64_t *row_offsets;  // grouped: [experts + 1] rows of operand A per expert
+  int experts;
+  int64_t sfb_expert_bytes;    // grouped: bytes of one expert's B scales
+  unsigned int *status;
+  long long wait_limit;
+};
+
+struct TileInfo {
+  int a_y, b_y;                // TMA row coordinates of the A and B tiles
+  const uint8_t *sfa_blk;      // first chunk of A's 128-row scale block
+  const uint8_t *sfb_blk;      // first chunk of B's first 128-row scale block
+  int sfb_blocks;              // B scale blocks present (<= SFB_BLOCKS)
+  int rows, cols;              // valid rows of A / of B in this tile
+  int64_t out_i0, out_j0;      // output coordinates of C[0][0] of the tile (before swap)
+  int kt0, kt1;                // K-stage range of this CTA
+};
+
+template <class C, bool GROUPED>
+struct Tables {
+  int *ro;   // [experts+1] row offsets (grouped only)
+  int *sfr;  // [experts+1] scale-row offsets (multiples of 128)
+  int *tp;   // [experts+1] tile prefix
+};
+
+template <class C, bool GROUPED>
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C, GROUPED> &tb,
+                                              int tile, int split) {
+  TileInfo t;
+  int64_t sfb_base_block;
+  if constexpr (GROUPED) {
+    int lo = 0, hi = p.experts - 1;  // largest e with tp[e] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tb.tp[mid] <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = lo;
+    const int rows_e = tb.ro[e + 1] - tb.ro[e];
+    const int mt_e = (rows_e + 127) / 128;
+    const int local = tile - tb.tp[e];
+    const int mt = local % mt_e, nt = local / mt_e;
+    t.a_y = tb.ro[e] + mt * 128;
+    t.b_y = e * p.n + nt * C::BN;
+    t.sfa_blk = p.sfa + (static_cast<int64_t>(tb.sfr[e] / 128 + mt) * p.sf_chunks) * 512;
+    sfb_base_block = (nt * C::BN) / 128;
+    t.sfb_blk = p.sfb + e * p.sfb_expert_bytes + sfb_base_block * p.sf_chunks * 512;
+    t.rows = min(128, rows_e - mt * 128);
+    t.cols = min(C::BN, p.n - nt * C::BN);
+    t.out_i0 = t.a_y;
+    t.out_j0 = nt * C::BN;
+    t.kt0 = 0;
+    t.kt1 = p.k_tiles;
+  } else {
+    const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+    t.a_y = mb * 128;
+    t.b_y = nb * C::BN;
+    t.sfa_blk = p.sfa + static_cast<int64_t>(mb) * p.sf_chunks * 512;
+    sfb_base_block = t.b_y / 128;
+    t.sfb_blk = p.sfb + sfb_base_block * p.sf_chunks * 512;
+    t.rows = min(128, p.m - t.a_y);
+    t.cols = min(C::BN, p.n - t.b_y);
+    t.out_i0 = t.a_y;
+    t.out_j0 = t.b_y;
+    t.kt0 = static_cast<int>(static_cast<int64_t>(split) * p.k_tiles / p.splits);
+    t.kt1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.k_tiles / p.splits);
+  }
+  t.sfb_blocks = min(C::SFB_BLOCKS, (t.cols + 127) / 128);
+  return t;
+}
+
+// Chunks / MMAs in K stage kt: the last stage may be short (K % 256 != 0).
+template <class C>
+__device__ __forceinline__ int stage_chunks(const GemmArgs &p, int kt) {
+  return min(C::CHUNKS, p.sf_chunks - kt * C::CHUNKS);
+}
+__device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
+  return min(4, (p.k - kt * 256 + 63) / 64);
+}
+
+template <class C, bool GROUPED>
+__global__ void __launch_bounds__(192, 1)
+    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *ctrl = smem + C::STAGES * C::STAGE_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(ctrl);
+  uint64_t *empty = full + C::STAGES;
+  uint64_t *accf = empty + C::STAGES;
+  uint64_t *acce = accf + 2;
+  uint64_t *drain = acce + 2;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+  volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
+  int *tables = reinterpret_cast<int *>(ctrl + C::CTRL_BYTES);
+  Tables<C, GROUPED> tb{tables, tables + (C::MAX_EXPERTS + 1), tables + 2 * (C::MAX_EXPERTS + 1)};
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const WaitCtl wc{p.wait_limit, abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&accf[a]), 1);
+      mbar_init(smem_u32(&acce[a]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    *consumed = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+
+  int total_tiles;
+  int tile0, tile_step, split = 0;
+  if constexpr (GROUPED) {
+    // Row offsets are produced by earlier kernels: read them only after the PDL wait.
+    pdl_wait();
+    const int E = p.experts;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) tb.ro[e] = static_cast<int>(p.row_offsets[e]);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int sfr = 0, tp = 0;
+      for (int e = 0; e < E; ++e) {
+        tb.sfr[e] = sfr;
+        tb.tp[e] = tp;
+        int cnt = tb.ro[e + 1] - tb.ro[e];
+        cnt = cnt < 0 ? 0 : cnt;
+        sfr += (cnt + 127) / 128 * 128;
+        tp += (cnt + 127) / 128 * p.n_tiles;
+      }
+      tb.sfr[E] = sfr;
+      tb.tp[E] = tp;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if constexpr (GROUPED) {
+    total_tiles = tb.tp[p.experts];
+    tile0 = blockIdx.x;
+    tile_step = gridDim.x;
+  } else {
+    if (p.splits > 1) {
+      total_tiles = p.m_tiles * p.n_tiles;
+      tile0 = blockIdx.x / p.splits;
+      split = blockIdx.x % p.splits;
+      tile_step = total_tiles;  // exactly one tile per CTA
+    } else {
+      total_tiles = p.m_tiles * p.n_tiles;
+      tile0 = blockIdx.x;
+      tile_step = gridDim.x;
+    }
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      pdl_wait();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+        for (int kt = t.kt0; kt < t.kt1; ++kt) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc)) goto producer_done;
+          const int nch = stage_chunks<C>(p, kt);
+          const uint32_t bytes = C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks);
+          uint8_t *st = smem + stage * C::STAGE_BYTES;
+          const uint32_t bar = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(bar, bytes);
+          tma_load_2d(smem_u32(st), &tmA, bar, kt * 128, t.a_y);
+          tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, bar, kt * 128, t.b_y);
+          uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
+          bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
+          for (int b = 0; b < t.sfb_blocks; ++b)
+            bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
+                      t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512,
+                      nch * 512, bar);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    producer_done:
+      pdl_trigger();
+      // remember how many stages were issued for the abort drain
+      reinterpret_cast<volatile int *>(tmem_holder)[3] = issued;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      uint32_t it = 0;
+      for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+        if (!mbar_wait(smem_u32(&acce[acc]), acc_phase ^ 1, wc)) goto mma_done;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * C::BN;
+        for (int kt = t.kt0; kt < t.kt1; ++kt, ++it) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, wc)) goto mma_done;
+          tc_fence_after();
+          *consumed = *consumed + 1;
+          const uint8_t *st = smem + stage * C::STAGE_BYTES;
+          const uint32_t a_s = smem_u32(st), b_s = smem_u32(st + C::A_BYTES);
+          const uint32_t sfa_s = smem_u32(st + C::A_BYTES + C::B_BYTES);
+          const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
+          const uint32_t slot = tmem + C::SF_COL0 + (it & 1) * C::SF_SLOT;
+          const int nch = stage_chunks<C>(p, kt);
+          for (int c = 0; c < nch; ++c) {
+            tc_cp_32x128b_x4(slot + 4 * c, sdesc_rows16(sfa_s + 512 * c));
+            for (int b = 0; b < t.sfb_blocks; ++b)
+              tc_cp_32x128b_x4(slot + C::SFA_COLS + c * 4 * C::SFB_BLOCKS + 4 * b,
+                               sdesc_rows16(sfb_s + (b * C::CHUNKS + c) * 512));
+          }
+          const int nmma = stage_mmas(p, kt);
+          const uint64_t adesc = sdesc_k_sw128(a_s), bdesc = sdesc_k_sw128(b_s);
+          for (int j = 0; j < nmma; ++j) {
+            const uint32_t accumulate = (kt > t.kt0 || j > 0) ? 1u : 0u;
+            if constexpr (C::MX) {
+              const int c = j >> 1;
+              const uint32_t id = (j & 1) * 2;
+              mma_mxf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC | (id << 29) | (id << 4),
+                       slot + 4 * c, slot + C::SFA_COLS + c * 4 * C::SFB_BLOCKS, accumulate);
+            } else {
+              mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j,
+                       slot + C::SFA_COLS + j * 4 * C::SFB_BLOCKS, accumulate);
+            }
+          }
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_commit(smem_u32(&accf[acc]));
+        if (++acc == C::NACC) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    mma_done:;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();
+    const int quad = warp & 3;  // tcgen05.ld: warp w reaches lanes 32*(w%4) .. +31
+    const int row = quad * 32 + lane;
+    const float alpha = p.alpha ? *p.alpha : 1.0f;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+      if (!mbar_wait(smem_u32(&accf[acc]), acc_phase, wc)) break;
+      tc_fence_after();
+      const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+      float *red = reinterpret_cast<float *>(smem);
+#pragma unroll 1
+      for (int c = 0; c < C::BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_base + 32 * c, r);
+        tmem_ld_wait();
+        if (p.splits > 1) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
+        } else if (!p.swap) {
+          if (row < t.rows && 32 * c < t.cols) {
+            __nv_bfloat16 *out = p.d + (t.out_i0 + row) * p.ldd + t.out_j0 + 32 * c;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                v[i] = pack_bf16x2(alpha * __uint_as_float(r[16 * h + 2 * i]),
+                                   alpha * __uint_as_float(r[16 * h + 2 * i + 1]));
+              st_global_v8(out + 16 * h, v);
+            }
+          }
+        } else if (row < t.rows) {
+          // operand A is the weight: TMEM lane = output column, TMEM column = output row
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int j = 32 * c + i;
+            if (j < t.cols) {
+              const float v = alpha * __uint_as_float(r[i]);
+              p.d[(t.out_j0 + j) * p.ldd + t.out_i0 + row] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce[acc]));
+      if (++acc == C::NACC) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // Drain: wait (bounded) for copies still landing in shared memory and for outstanding
+    // tcgen05 operations, so nothing writes shared or tensor memory after the CTA is gone.
+    if (threadIdx.x == 0) {
+      const int issued = reinterpret_cast<volatile int *>(tmem_holder)[3];
+      const int done = *consumed;
+      for (int i = (done > issued - C::STAGES ? done : issued - C::STAGES); i < issued; ++i) {
+        const uint32_t bar = smem_u32(&full[i % C::STAGES]);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, (i / C::STAGES) & 1) && clock64() - t0 < p.wait_limit) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {
+      tc_commit(smem_u32(drain));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < p.wait_limit) {
+      }
+    }
+    __syncthreads();
+  }
+
+  if constexpr (!GROUPED) {
+    if (p.splits > 1) {
+      // Split-K reduction across the cluster: CTA `rank` owns columns [c0, c1) of the tile.
+      cluster_sync();
+      if (warp >= 2) {
+        const int row = threadIdx.x - 64;  // 0..127
+        const int rank = static_cast<int>(cluster_ctarank());
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile0, split);
+        const float alpha = p.alpha ? *p.alpha : 1.0f;
+        const int per = (C::BN + p.splits - 1) / p.splits;
+        const int c0 = rank * per, c1 = min(C::BN, c0 + per);
+        const uint32_t red0 = smem_u32(smem);
+        for (int c = c0; c < c1; ++c) {
+          const uint32_t off = red0 + static_cast<uint32_t>((c * 128 + row) * 4);
+          float v = 0.0f;
+          for (int s = 0; s < p.splits; ++s) v += ld_cluster_f32(map_to_rank(off, s));
+          if (row < t.rows && c < t.cols) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(alpha * v);
+            if (p.swap) p.d[(t.out_j0 + c) * p.ldd + t.out_i0 + row] = b;
+            else p.d[(t.out_i0 + row) * p.ldd + t.out_j0 + c] = b;
+          }
+        }
+      }
+      cluster_sync();
+    }
+  }
+
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace nvfp4

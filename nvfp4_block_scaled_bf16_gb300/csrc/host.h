@@ -1,0 +1,74 @@
+// Host-side helpers shared by the entry points: error reporting, device checks, launches.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <utility>
+
+#include "nvfp4.h"
+
+namespace nvfp4 {
+
+// Records a formatted message for nvfp4_last_error() and returns `code`.
+nvfp4_status_t fail(nvfp4_status_t code, const char *fmt, ...);
+void clear_error();
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  unsigned int *status;  // device status word (address of a __device__ variable)
+};
+// Checks that the current device is sm_103 and returns its cached properties.
+nvfp4_status_t current_device(DeviceInfo *out);
+
+// Wait limit (SM clock cycles) for the bounded pipeline waits.
+long long wait_limit(uint32_t flags);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda needed).
+nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes,
+                                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                                 uint32_t box_rows, bool swizzle128);
+
+// Raises the dynamic shared-memory limit of `fn` on the current device (once per device).
+nvfp4_status_t allow_smem(const void *fn, int bytes, int device);
+
+inline bool aligned(const void *p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+inline int64_t round_up(int64_t x, int64_t y) { return (x + y - 1) / y * y; }
+inline int64_t ceil_div(int64_t x, int64_t y) { return (x + y - 1) / y; }
+
+// cudaLaunchKernelEx with optional programmatic-dependent-launch and cluster attributes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                   bool pdl, int cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  unsigned n = 0;
+  if (pdl) {
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+nvfp4_status_t check_launch(cudaError_t e, const char *what);
+
+}  // namespace nvfp4

@@ -1,0 +1,99 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports every entry point
+include/nvfp4.h declares, answers the size queries, and rejects bad arguments before it touches
+a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_bf16_gb300 as nv
+    return nv
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:nvfp4|mxfp4|sf)_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for want in ("nvfp4_quantize", "nvfp4_gemm", "mxfp4_quantize", "mxfp4_grouped_gemm", "sf_swizzle",
+                 "nvfp4_last_error", "nvfp4_sf_bytes", "nvfp4_check_status", "nvfp4_gemm_plan"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for name in _declared():
+        assert hasattr(raw, name), name
+
+
+def test_size_queries(lib):
+    assert lib.sf_bytes(1, 16, 16) == 128 * 4
+    assert lib.sf_bytes(32, 1024, 16) == 128 * 64
+    assert lib.sf_bytes(129, 7168, 16) == 256 * 448
+    assert lib.sf_bytes(5, 96, 16) == 128 * 8
+    assert lib.sf_bytes(300, 2048, 32) == 384 * 64
+    assert lib.sf_bytes(-1, 16, 16) == 0
+    assert lib.sf_bytes(4, 24, 16) == 0
+    assert lib.sf_bytes(4, 32, 8) == 0
+    assert lib.grouped_sf_bytes(32768, 128, 2048) == (32768 + 128 * 128) * 64
+    assert lib.grouped_sf_bytes(10, 0, 64) == 0
+
+
+def test_plan_selector_buckets(lib):
+    for m in (1, 4, 8, 16):
+        p = lib.nvfp4_gemm_plan(m, 4096, 7168)
+        assert p["swap_ab"] == 1 and p["tile_n"] == 16 and 1 <= p["splits"] <= 8
+    assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
+    assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
+    big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
+    assert big["swap_ab"] == 0 and big["splits"] == 1 and big["ctas"] <= 152
+    for m in (1, 32, 256, 1024, 4096):
+        p = lib.nvfp4_gemm_plan(m, 4096, 7168)
+        assert p["ctas"] >= 1 and p["stages"] >= 2
+
+
+def _c(v):
+    return ctypes.c_void_p(v)
+
+
+def test_gemm_rejects_bad_arguments_without_a_device(lib):
+    L = lib.lib
+    A, S, D = 0x10000, 0x20000, 0x30000  # never dereferenced: validation fails first
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1000, 0, None) == 3  # k % 32
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1000, 1024, 0, None) == 3  # n % 32
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), -1, 1024, 1024, 0, None) == 1
+    assert L.nvfp4_gemm(None, _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 1
+    assert L.nvfp4_gemm(_c(A + 16), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 2
+    assert L.nvfp4_gemm(_c(A), _c(S + 8), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 2
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 1 << 20, None) == 1
+    assert "k" in lib.last_error() or "flags" in lib.last_error()
+    # zero rows: a legal no-op that needs no device
+    assert L.nvfp4_gemm(None, None, None, None, None, None, 0, 1024, 1024, 0, None) == 0
+
+
+def test_quantizers_reject_bad_arguments_without_a_device(lib):
+    L = lib.lib
+    X, G, Q, S = 0x10000, 0x20000, 0x30000, 0x40000
+    assert L.nvfp4_quantize(_c(X), 4, 24, 24, _c(G), _c(Q), _c(S), 0, None) == 3     # k % 16
+    assert L.nvfp4_quantize(_c(X), 4, 32, 20, _c(G), _c(Q), _c(S), 0, None) == 2     # ldx < k
+    assert L.nvfp4_quantize(_c(X + 2), 4, 32, 32, _c(G), _c(Q), _c(S), 0, None) == 2
+    assert L.nvfp4_quantize(None, 4, 32, 32, _c(G), _c(Q), _c(S), 0, None) == 1
+    assert L.nvfp4_quantize(None, 0, 32, 32, None, None, None, 0, None) == 0
+    assert L.mxfp4_quantize(_c(X), 4, 48, 48, None, 0, _c(Q), _c(S), 1 << 20, 0, None) == 3
+    assert L.mxfp4_quantize(_c(X), 4, 64, 64, None, 0, _c(Q), _c(S), 16, 0, None) == 1   # sf too small
+    assert L.mxfp4_quantize(_c(X), 4, 64, 64, _c(X), 2000, _c(Q), _c(S), 1 << 30, 0, None) == 1
+    assert L.mxfp4_grouped_gemm(_c(X), _c(S), _c(X), 0, _c(X), _c(S), None, _c(Q), 4, 64, 64, 0, None) == 1
+    assert L.sf_swizzle(_c(X), _c(Q), -1, 4, 1, None) == 1
+    assert L.sf_swizzle(_c(X), _c(Q), 4, 4, 7, None) == 1

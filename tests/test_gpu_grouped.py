@@ -1,0 +1,72 @@
+"""GPU parity of the MXFP4 grouped (MoE) GEMM against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from cases import assert_within, dev, scalar
+from oracle import gemm as ogemm
+from oracle import quant as oquant
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_bf16_gb300 as m
+    return m
+
+
+def _weights(seed, E, n, k):
+    xb = synth.weight(seed, n, k, experts=E)
+    qb = np.empty((E, n, k // 2), dtype=np.uint8)
+    sfb = []
+    for e in range(E):
+        q, s = oquant.mxfp4_quantize(xb[e])
+        qb[e] = q
+        sfb.append(s)
+    return qb, np.stack(sfb)
+
+
+def _check(nv, counts, n, k, seed=0, alpha=None, experts_to_check=None):
+    counts = torch.as_tensor(counts, dtype=torch.int64)
+    E = counts.numel()
+    ro, _ = synth.moe_offsets(counts)
+    t = int(ro[-1])
+    xa = synth.activation(seed, t, k)
+    qa, sfa = oquant.mxfp4_quantize(xa, ro.numpy())
+    qb, sfb = _weights(seed, E, n, k)
+    sfa_d = torch.zeros(nv.grouped_sf_bytes(t, E, k), dtype=torch.uint8, device="cuda")
+    sfa_d[:sfa.size] = dev(sfa)
+    d = nv.mxfp4_grouped_gemm(dev(qa), sfa_d, ro.cuda(), dev(qb), dev(sfb),
+                              None if alpha is None else scalar(alpha))
+    torch.cuda.synchronize()
+    nv.check_status()
+    out = ogemm.mxfp4_grouped_gemm(qa, sfa, ro.numpy(), qb, sfb, alpha, n, k, experts_to_check)
+    for e, (Ae, Be, Re) in out.items():
+        r0, r1 = int(ro[e]), int(ro[e + 1])
+        if r1 == r0:
+            continue
+        tol = ogemm.tolerance(Re, ogemm.abs_product_sum(Ae, Be, 1.0 if alpha is None else alpha))
+        assert_within(d[r0:r1], Re, tol, f"expert {e}")
+    return d
+
+
+def test_small_groups_with_empty_experts(nv):
+    _check(nv, [3, 0, 130, 1, 0, 256, 129], 256, 512)
+
+
+def test_alpha_and_k_tail(nv):
+    _check(nv, [5, 200, 64], 128, 96 * 2, alpha=0.25)
+
+
+def test_moe_gate_up_sampled_experts(nv):
+    """E=128 experts, 4096 tokens top-8 (32768 rows), gate+up N=1536, K=2048; the oracle checks
+    the smallest and largest experts and six seeded others."""
+    counts = synth.moe_routing(0, 4096, 128, 8)
+    order = torch.argsort(counts)
+    rng = np.random.default_rng(0)
+    pick = sorted(set([int(order[0]), int(order[-1])] + [int(v) for v in rng.integers(0, 128, 6)]))
+    _check(nv, counts, 1536, 2048, experts_to_check=pick)
