@@ -4,7 +4,7 @@ Thin ctypes marshalling over the C ABI in include/nvfp4.h: each function here ha
 the C entry point it calls, takes torch CUDA tensors, allocates missing outputs with
 torch.empty, and passes raw pointers and the current CUDA stream.  All arithmetic runs in the
 library's CUDA kernels; there is no CPU fallback.  Importing fails if libnvfp4.so is missing
-(build it with ``python -m nvfp4_block_scaled_bf16_gb300.build``).
+(build it with ``python nvfp4_block_scaled_bf16_gb300/build.py``).
 """
 from __future__ import annotations
 
@@ -15,7 +15,7 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4.so")
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"{_LIB_PATH} is not built: run `python -m nvfp4_block_scaled_bf16_gb300.build`")
+    raise ImportError(f"{_LIB_PATH} is not built: run `python nvfp4_block_scaled_bf16_gb300/build.py`")
 _lib = ctypes.CDLL(_LIB_PATH)
 
 _i64, _u32, _int, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t

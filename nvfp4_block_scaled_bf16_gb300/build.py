@@ -1,6 +1,6 @@
 """Builds libnvfp4.so (the C-ABI library) in place with nvcc, for sm_103a only.
 
-    python -m nvfp4_block_scaled_bf16_gb300.build
+    python nvfp4_block_scaled_bf16_gb300/build.py
 
 Each translation unit under csrc/ is compiled in parallel, then linked against the shared CUDA
 runtime (the one PyTorch already loaded, so streams and contexts are shared).

@@ -125,16 +125,20 @@ nvfp4_status_t allow_smem(const void *fn, int bytes, int device) {
         return NVFP4_OK;
   }
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess)
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // consume the error this call raised so later calls do not see it
     return fail(NVFP4_ERR_CUDA, "cudaFuncSetAttribute(smem=%d): %s", bytes, cudaGetErrorString(e));
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_smem_n < 256) g_smem[g_smem_n++] = SmemEntry{fn, device, bytes};
   return NVFP4_OK;
 }
 
 nvfp4_status_t check_launch(cudaError_t e, const char *what) {
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // a failed launch also records itself as the runtime's last error
+    return fail(NVFP4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  }
   return NVFP4_OK;
 }
 

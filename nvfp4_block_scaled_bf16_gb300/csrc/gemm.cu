@@ -4,8 +4,8 @@
 // nvfp4_scaled_mm_kernels.cu, which buckets M into [1,16], (16,256], (256,inf); and of the
 // narrow output tiles FlashInfer PR 4865's "Reviewer Notes" credit for small-M speed):
 //   M <= 256  swap A and B: the weight's rows fill the 128-row MMA slot and the tokens the
-//             N slot (N = round_up(M,16) up to 128, else 256), so no MMA row is wasted on
-//             padding; K is split over a thread-block cluster of up to 8 CTAs until the
+//             N slot (N = 32, 64, 128 or 256, the smallest that holds M), so no MMA row is
+//             wasted on padding; K is split over a thread-block cluster of up to 8 CTAs until the
 //             grid covers the SMs, and the partial tiles are reduced through distributed
 //             shared memory (decode shapes are weight-streaming, so every SM must pull).
 //   M >  256  128 x 256 tiles (128 x 128 when N is not a multiple of 256... or fewer tiles
@@ -26,7 +26,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   pl.k_tiles = static_cast<int>(ceil_div(k, 256));
   if (m <= 256) {
     pl.swap = 1;
-    pl.bn = m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
+    pl.bn = m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
     pl.m_tiles = static_cast<int>(ceil_div(n, 128));  // weight rows
     pl.n_tiles = static_cast<int>(ceil_div(m, pl.bn));
     const int tiles = pl.m_tiles * pl.n_tiles;
@@ -45,7 +45,6 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     pl.ctas = tiles < sm_count ? tiles : sm_count;
   }
   switch (pl.bn) {
-    case 16: pl.stages = 8; break;
     case 32: pl.stages = 8; break;
     case 64: pl.stages = 7; break;
     case 128: pl.stages = 6; break;
@@ -59,9 +58,9 @@ nvfp4_status_t run(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb,
                    const DeviceInfo &dev, uint32_t flags, cudaStream_t s) {
   using C = GemmCfg<BN, STAGES, false>;
   auto kern = bs_gemm_kernel<C, false>;
-  nvfp4_status_t st = allow_smem(reinterpret_cast<const void *>(kern), C::SMEM_BYTES, dev.device);
+  nvfp4_status_t st = allow_smem(reinterpret_cast<const void *>(kern), C::smem_bytes(false), dev.device);
   if (st != NVFP4_OK) return st;
-  cudaError_t e = launch(kern, dim3(pl.ctas), dim3(192), C::SMEM_BYTES, s,
+  cudaError_t e = launch(kern, dim3(pl.ctas), dim3(192), C::smem_bytes(false), s,
                          (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, args);
   return check_launch(e, "nvfp4_gemm");
 }
@@ -138,7 +137,6 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
 
   cudaStream_t s = (cudaStream_t)stream;
   switch (pl.bn) {
-    case 16: return run<16, 8>(pl, ta, tb, args, dev, flags, s);
     case 32: return run<32, 8>(pl, ta, tb, args, dev, flags, s);
     case 64: return run<64, 7>(pl, ta, tb, args, dev, flags, s);
     case 128: return run<128, 6>(pl, ta, tb, args, dev, flags, s);

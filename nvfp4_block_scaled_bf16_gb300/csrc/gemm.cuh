@@ -56,11 +56,14 @@ struct GemmCfg {
   static constexpr int MAX_EXPERTS = 1024;
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
   static constexpr int CTRL_BYTES = 256;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + CTRL_BYTES + TABLE_BYTES;
+  // dynamic shared memory: alignment slack, stage ring, barriers, expert tables (grouped only)
+  static constexpr int smem_bytes(bool grouped) {
+    return 1024 + STAGES * STAGE_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
+  }
   static constexpr uint32_t IDESC = idesc_block_scaled(BM, BN, MX, 0);
   static_assert(TMEM_USED <= 512, "tensor memory budget");
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(STAGE_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
 };
 

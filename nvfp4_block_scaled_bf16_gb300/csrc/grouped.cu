@@ -70,12 +70,12 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
   args.wait_limit = wait_limit(flags);
 
   auto kern = bs_gemm_kernel<GroupedCfg, true>;
-  st = allow_smem(reinterpret_cast<const void *>(kern), GroupedCfg::SMEM_BYTES, dev.device);
+  st = allow_smem(reinterpret_cast<const void *>(kern), GroupedCfg::smem_bytes(true), dev.device);
   if (st != NVFP4_OK) return st;
   // Upper bound of the work list: sum_e ceil(M_e/128) <= ceil(t/128) + experts.
   const int64_t max_tiles = (ceil_div(t, 128) + num_experts) * args.n_tiles;
   const int grid = static_cast<int>(max_tiles < dev.sm_count ? max_tiles : dev.sm_count);
-  cudaError_t e = launch(kern, dim3(grid), dim3(192), GroupedCfg::SMEM_BYTES, (cudaStream_t)stream,
+  cudaError_t e = launch(kern, dim3(grid), dim3(192), GroupedCfg::smem_bytes(true), (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, ta, tb, args);
   return check_launch(e, "mxfp4_grouped_gemm");
 }

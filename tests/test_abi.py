@@ -54,7 +54,7 @@ def test_size_queries(lib):
 def test_plan_selector_buckets(lib):
     for m in (1, 4, 8, 16):
         p = lib.nvfp4_gemm_plan(m, 4096, 7168)
-        assert p["swap_ab"] == 1 and p["tile_n"] == 16 and 1 <= p["splits"] <= 8
+        assert p["swap_ab"] == 1 and p["tile_n"] == 32 and 1 <= p["splits"] <= 8
     assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
     big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
