@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 quantise -> GEMM hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|e2e|moe]
+    python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
+
+Workloads (synthetic, seeded; shapes and value distributions of the pages' benchmarks):
+  decode   (default)  N=4096, K=7168, M in {1,4,8,16,32,64,128,256}.  One step quantises the
+                      bf16 activation of every M on the device and multiplies it with its own
+                      copy of the NVFP4 weight (8 distinct copies, 132 MB, so no GEMM finds its
+                      weight in L2), quant and GEMM chained with programmatic dependent launch.
+  prefill             (M,N,K) in {(1024,4096,7168), (2048,4096,7168), (4096,4096,7168),
+                      (4096,4096,4096), (128,7168,2048)}, quant -> GEMM per shape.
+  e2e                 bf16 activation [M,4096], M in {256,512}, weights [14336,4096]: quant ->
+                      GEMM with PDL; the line also carries the time without PDL.
+  moe                 MXFP4: 4096 tokens top-8 over 128 experts (32768 rows); quantise, then the
+                      gate+up grouped GEMM (N=1536, K=2048) and the down grouped GEMM (N=2048,
+                      K=768) on a second quantised activation.
+Each step is captured once in a CUDA graph and replayed; the L2 is flushed (a 512 MB write)
+before every timed step, outside the timed interval.  `value` is GEMM TFLOPS over the whole
+step (quantisation time included); `roofline` covers the GEMM kernel, timed on its own in a
+second graph of the step's GEMM launches.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "NVFP4 GEMM TFLOPS and % of binding roofline (FP4 peak or 8 TB/s HBM) vs M"
+DECODE_MS = (1, 4, 8, 16, 32, 64, 128, 256)
+PREFILL = ((1024, 4096, 7168), (2048, 4096, 7168), (4096, 4096, 7168), (4096, 4096, 4096), (128, 7168, 2048))
+# FlashInfer PR 4865 B300 table (best of its SM100/SM103 kernels, ms), N=4096 K=7168: context only
+PAGES_B300_DECODE_MS = {1: 0.0100, 4: 0.0099, 8: 0.0096, 16: 0.0097, 32: 0.0097, 64: 0.0094, 128: 0.0096, 256: 0.0091}
+
+
+def gemm_bytes(m, n, k):
+    """Algorithmic bytes of one NVFP4 GEMM: packed A and B, their scales (unpadded), bf16 D."""
+    return m * k // 2 + m * k // 16 + n * k // 2 + n * k // 16 + 2 * m * n
+
+
+def grouped_bytes(experts, t, n, k):
+    return experts * n * k * (1 / 2 + 1 / 32) + t * k * (1 / 2 + 1 / 32) + 2 * t * n
+
+
+def quant_bytes(m, k, vec=16):
+    return 2 * m * k + m * k // 2 + m * k // vec
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampler (every 200 ms) around the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        args = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].strip()
+        self.index = vis if vis.isdigit() else None   # nvidia-smi index of the GPU in use
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(args, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        self.p.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            rows = [[x.strip() for x in line.split(",")] for line in f]
+        indices = sorted({r[0] for r in rows if len(r) >= 9})
+        want = self.index if self.index in indices else (indices[0] if indices else None)
+        for parts in rows:
+            if len(parts) < 9 or parts[0] != want:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- workloads
+class Workload:
+    """Holds device buffers and knows how to run one step (quant -> GEMM chain)."""
+
+    def __init__(self, nv, name: str):
+        self.nv, self.name = nv, name
+        self.launches = []         # callables, in order, each one kernel
+        self.gemm_launches = []    # the GEMM kernels alone (roofline pass)
+        self.flops = 0.0
+        self.gemm_bytes = 0.0
+        self.quant_bytes = 0.0
+        self.h2d = []              # (device tensor, pinned host tensor) per step input
+        self.d2h = []              # (host tensor, device tensor) per step output
+        self.config = {}
+        self.extra = {}
+
+    def step(self):
+        for f in self.launches:
+            f()
+
+
+def _gs(x: torch.Tensor) -> float:
+    return float(np.float32(2688.0) / np.float32(x.float().abs().max().item()))
+
+
+def build_nvfp4_chain(nv, wl: Workload, shapes, weight_seed=0, weights_by_shape=None, pdl=True):
+    flags = nv.FLAG_PDL if pdl else 0
+    cache = {}
+    for i, (m, n, k) in enumerate(shapes):
+        key = (n, k)
+        if key not in cache:
+            w = synth.weight(weight_seed, n, k)
+            gsw = _gs(w)
+            qb, sfb = nv.nvfp4_quantize(w.cuda(), torch.tensor([gsw], device="cuda"))
+            cache[key] = (qb, sfb, gsw)
+        qb, sfb, gsw = cache[key]
+        qb, sfb = qb.clone(), sfb.clone()          # every GEMM streams its own weight copy
+        x = synth.activation(i, m, k)
+        gsa = _gs(x)
+        xd = x.cuda()
+        gs_d = torch.tensor([gsa], dtype=torch.float32, device="cuda")
+        al_d = torch.tensor([float(np.float32(1.0) / (np.float32(gsa) * np.float32(gsw)))], device="cuda")
+        q = torch.empty((m, k // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.empty(nv.sf_bytes(m, k), dtype=torch.uint8, device="cuda")
+        d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        wl.launches.append(lambda xd=xd, gs_d=gs_d, q=q, sf=sf: nv.nvfp4_quantize(xd, gs_d, q, sf, flags=flags))
+        g = (lambda q=q, sf=sf, qb=qb, sfb=sfb, al_d=al_d, d=d, f=flags: nv.nvfp4_gemm(q, sf, qb, sfb, al_d, d, flags=f))
+        wl.launches.append(g)
+        wl.gemm_launches.append(g)
+        wl.flops += 2.0 * m * n * k
+        wl.gemm_bytes += gemm_bytes(m, n, k)
+        wl.quant_bytes += quant_bytes(m, k)
+        wl.h2d.append((xd, x.pin_memory()))
+        wl.d2h.append((torch.empty((m, n), dtype=torch.bfloat16).pin_memory(), d))
+
+
+def make_decode(nv):
+    wl = Workload(nv, "decode")
+    build_nvfp4_chain(nv, wl, [(m, 4096, 7168) for m in DECODE_MS])
+    wl.config = {"workload": "decode sweep: NVFP4 quant->GEMM, N=4096 K=7168, M in 1,4,8,16,32,64,128,256",
+                 "global_batch": sum(DECODE_MS), "n": 4096, "k": 7168, "ms": list(DECODE_MS),
+                 "inputs": "activation N(0,1) with 0.1% outlier channels x20, weight N(0,0.02), seed 0",
+                 "l2": "flushed (512 MB write) before every timed step; 8 distinct weight copies",
+                 "parallelism": "replicas"}
+    return wl
+
+
+def make_prefill(nv):
+    wl = Workload(nv, "prefill")
+    build_nvfp4_chain(nv, wl, list(PREFILL))
+    wl.config = {"workload": "prefill sweep: NVFP4 quant->GEMM, (M,N,K) in " + str(list(PREFILL)),
+                 "global_batch": sum(s[0] for s in PREFILL),
+                 "inputs": "activation N(0,1) with 0.1% outlier channels x20, weight N(0,0.02), seed 0",
+                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+    return wl
+
+
+def make_e2e(nv, pdl=True):
+    wl = Workload(nv, "e2e")
+    build_nvfp4_chain(nv, wl, [(256, 14336, 4096), (512, 14336, 4096)], pdl=pdl)
+    wl.config = {"workload": "quant->GEMM with PDL: act bf16 [M,4096], M in 256,512, weight [14336,4096]",
+                 "global_batch": 768, "pdl": pdl,
+                 "inputs": "activation N(0,1) with outlier channels x20, weight N(0,0.02), seed 0",
+                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+    return wl
+
+
+def make_moe(nv):
+    wl = Workload(nv, "moe")
+    E, T, topk, H, I = 128, 4096, 8, 2048, 768
+    counts = synth.moe_routing(0, T, E, topk)
+    ro, _ = synth.moe_offsets(counts)
+    rows = int(ro[-1])
+    ro_d = ro.cuda()
+    specs = [("gate_up", 2 * I, H, 1), ("down", H, I, 2)]
+    for name, n, k, seed in specs:
+        wb = synth.weight(seed, n, k, experts=E)
+        qb = torch.empty((E, n, k // 2), dtype=torch.uint8, device="cuda")
+        sfb = torch.empty((E, nv.sf_bytes(n, k, 32)), dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            nv.mxfp4_quantize(wb[e].cuda(), q=qb[e], sf=sfb[e])
+        del wb
+        x = synth.activation(seed + 10, rows, k, outliers=False)
+        xd = x.cuda()
+        q = torch.empty((rows, k // 2), dtype=torch.uint8, device="cuda")
+        sf = torch.zeros(nv.grouped_sf_bytes(rows, E, k), dtype=torch.uint8, device="cuda")
+        d = torch.empty((rows, n), dtype=torch.bfloat16, device="cuda")
+        fl = nv.FLAG_PDL
+        wl.launches.append(lambda xd=xd, q=q, sf=sf: nv.mxfp4_quantize(xd, ro_d, q, sf, flags=fl))
+        g = (lambda q=q, sf=sf, qb=qb, sfb=sfb, d=d: nv.mxfp4_grouped_gemm(q, sf, ro_d, qb, sfb, None, d, flags=fl))
+        wl.launches.append(g)
+        wl.gemm_launches.append(g)
+        wl.flops += 2.0 * rows * n * k
+        wl.gemm_bytes += grouped_bytes(E, rows, n, k)
+        wl.quant_bytes += quant_bytes(rows, k, 32)
+        wl.h2d.append((xd, x.pin_memory()))
+        wl.d2h.append((torch.empty((rows, n), dtype=torch.bfloat16).pin_memory(), d))
+    wl.config = {"workload": "MXFP4 MoE: 128 experts, 4096 tokens top-8 (32768 rows); gate+up N=1536 K=2048, "
+                             "down N=2048 K=768; quant + grouped GEMM each",
+                 "global_batch": rows, "expert_rows_min": int(counts.min()), "expert_rows_max": int(counts.max()),
+                 "inputs": "activation N(0,1), weight N(0,0.02), router logits N(0,1), seed 0",
+                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+    return wl
+
+
+def make_custom(nv, shapes):
+    wl = Workload(nv, "custom")
+    build_nvfp4_chain(nv, wl, shapes)
+    wl.config = {"workload": "NVFP4 quant->GEMM chain " + str(shapes), "global_batch": sum(s[0] for s in shapes),
+                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+    return wl
+
+
+MAKERS = {"decode": make_decode, "prefill": make_prefill, "e2e": make_e2e, "moe": make_moe}
+
+
+# ---------------------------------------------------------------------------- timing
+def capture(fns) -> torch.cuda.CUDAGraph:
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for f in fns:   # warm-up outside capture: kernel attributes, module load
+            f()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed_replays(g, n: int, flush: torch.Tensor, before=None, after=None) -> list[float]:
+    """Per-replay device times (ms), each after an L2 flush outside the timed interval."""
+    out = []
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        a, b = evs[i]
+        a.record()
+        if before:
+            before()
+        g.replay()
+        if after:
+            after()
+        b.record()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        out.append(a.elapsed_time(b))
+    return out
+
+
+def barrier(dist_on: bool):
+    if dist_on:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(v: float, dist_on: bool) -> float:
+    if not dist_on:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, dist_on, rank, world):
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_bf16_gb300 as nv
+
+    if args.shapes:
+        shapes = [tuple(int(v) for v in s.split(",")) for s in args.shapes.split(";")]
+        wl = make_custom(nv, shapes)
+    else:
+        wl = MAKERS[args.workload](nv)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    step_graph = capture(wl.launches)
+    gemm_graph = capture(wl.gemm_launches)
+    for _ in range(args.warmup):
+        step_graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    clocks = Clocks(torch.cuda.current_device())
+    barrier(dist_on)
+    t_wall = time.perf_counter()
+    step_ms = timed_replays(step_graph, args.steps, flush)
+    barrier(dist_on)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dist_on)
+
+    # ---- GEMM kernels alone (roofline of the dominant kernel)
+    gemm_ms = timed_replays(gemm_graph, max(3, args.steps), flush)
+    per_launch_ms = statistics.median(gemm_ms) / len(wl.gemm_launches)
+    quant_ms = max(0.0, ms - statistics.median(gemm_ms))
+
+    # ---- end to end through the public API with host buffers
+    def h2d():
+        for dev_t, host_t in wl.h2d:
+            dev_t.copy_(host_t, non_blocking=True)
+
+    def d2h():
+        for host_t, dev_t in wl.d2h:
+            host_t.copy_(dev_t, non_blocking=True)
+
+    e2e_ms_list = timed_replays(step_graph, args.steps, flush, before=h2d, after=d2h)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_ms_list), dist_on)
+    h2d_bytes = sum(t.numel() * t.element_size() for _, t in wl.h2d)
+    d2h_bytes = sum(t.numel() * t.element_size() for t, _ in wl.d2h)
+
+    hbm, bf16, peak_kind = peaks()
+    tflops = wl.flops * world / (ms * 1e-3) / 1e12
+    gemm_gbs = wl.gemm_bytes / (statistics.median(gemm_ms) * 1e-3) / 1e9
+    fp4_peak_tflops = bf16 * 6.0  # nominal dense FP4 : bf16 ratio 13.5 : 2.25
+    gemm_tflops = wl.flops / (statistics.median(gemm_ms) * 1e-3) / 1e12
+    # binding roof of the step's GEMMs: max(flops / FP4 peak, bytes / HBM)
+    t_roof = max(wl.flops / (fp4_peak_tflops * 1e12), wl.gemm_bytes / (hbm * 1e9))
+    bound = "hbm" if wl.gemm_bytes / (hbm * 1e9) >= wl.flops / (fp4_peak_tflops * 1e12) else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gemm_gbs / hbm, 4), "traffic": None}
+    else:
+        roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak_tflops, 1),
+                "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak_tflops, 4), "traffic": None}
+    roof.update({"kernel": "bs_gemm_kernel" if wl.name != "moe" else "bs_gemm_kernel (grouped)",
+                 "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if bound == 'hbm' else 'bf16_tflops x 6, the nominal fp4/bf16 ratio'})",
+                 "per_launch_ms": round(per_launch_ms, 5), "binding_roof_frac": round(t_roof / (statistics.median(gemm_ms) * 1e-3), 4),
+                 "bytes_per_step": wl.gemm_bytes})
+
+    line = {"metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4 (e2m1) x fp4, fp32 accumulate, bf16 out",
+            "data": "synthetic", "config": wl.config,
+            "roofline": roof,
+            "e2e": {"value": round(wl.flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+                    "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
+            "gpu_launches": len(wl.launches) * args.steps,
+            "clocks": clk,
+            "breakdown": {"gemm_ms": round(statistics.median(gemm_ms), 5), "quant_ms_est": round(quant_ms, 5),
+                          "quant_bytes_per_step": wl.quant_bytes, "wall_s": round(wall, 3)}}
+    if wl.name == "decode":
+        line["pages_b300_context"] = {
+            "gemm_only_ms_sum": round(sum(PAGES_B300_DECODE_MS.values()), 4),
+            "note": "FlashInfer PR 4865 B300 best-kernel times for the same 8 GEMMs (GEMM only, other machine)"}
+    if wl.name == "e2e":
+        nopdl = make_e2e(nv, pdl=False)
+        g2 = capture(nopdl.launches)
+        for _ in range(args.warmup):
+            g2.replay()
+        t2 = timed_replays(g2, args.steps, flush)
+        line["without_pdl_ms_per_step"] = round(max_over_ranks(statistics.mean(t2), dist_on), 5)
+    if rank == 0:
+        line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(args.workload)
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_step(workload: str, n_rows_sample: int):
+    """One bounded sample of the workload through the CPU oracle (quantise both operands,
+    dequantise, fp64 GEMM); returns (flops done, seconds, description)."""
+    from oracle import gemm as ogemm
+    from oracle import quant as oquant
+    if workload == "moe":
+        shapes = [(256, 1536, 2048), (256, 2048, 768)]     # one average expert, both GEMMs
+        desc = "one 256-row expert of each MoE GEMM (gate+up 1536x2048, down 2048x768), MXFP4"
+    elif workload == "prefill":
+        shapes = [(64, n_rows_sample, k) for (_, n, k) in PREFILL]
+        desc = f"64 activation rows x {n_rows_sample} weight rows of each prefill shape"
+    elif workload == "e2e":
+        shapes = [(m, n_rows_sample, 4096) for m in (256, 512)]
+        desc = f"both e2e M, {n_rows_sample} of 14336 weight rows"
+    else:
+        shapes = [(m, n_rows_sample, 7168) for m in DECODE_MS]
+        desc = f"all 8 decode M, {n_rows_sample} of 4096 weight rows, K=7168"
+    flops = 0.0
+    t0 = time.perf_counter()
+    for i, (m, n, k) in enumerate(shapes):
+        xa = synth.activation(i, m, k)
+        xb = synth.weight(0, n, k)
+        if workload == "moe":
+            qa, sfa = oquant.mxfp4_quantize(xa)
+            qb, sfb = oquant.mxfp4_quantize(xb)
+            A = ogemm.dequantize(qa, sfa, m, k, 32, "ue8m0")
+            B = ogemm.dequantize(qb, sfb, n, k, 32, "ue8m0")
+            _ = A @ B.T
+        else:
+            gsa = np.float32(2688.0) / np.float32(xa.float().abs().max().item())
+            gsb = np.float32(2688.0) / np.float32(xb.float().abs().max().item())
+            qa, sfa = oquant.nvfp4_quantize(xa, gsa)
+            qb, sfb = oquant.nvfp4_quantize(xb, gsb)
+            _ = ogemm.nvfp4_gemm(qa, sfa, qb, sfb, np.float32(1.0) / (gsa * gsb), m, n, k)
+        flops += 2.0 * m * n * k
+    return flops, time.perf_counter() - t0, desc
+
+
+def cpu_baseline(workload: str) -> dict:
+    flops, secs, desc = oracle_step(workload, 1024)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOPS", "cores": _cores(), "kind": "oracle",
+            "sample": desc + f" ({secs:.1f} s, numpy fp64)"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_step(args.workload, 128)
+    total_f, total_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s, desc = oracle_step(args.workload, 128)
+        total_f += f
+        total_s += s
+    v = total_f / total_s / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "TFLOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload} (bounded sample through the CPU oracle)", "sample": desc},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOPS", "cores": _cores(), "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(MAKERS), default="decode")
+    ap.add_argument("--shapes", default="", help="custom quant->GEMM chain, e.g. '32,4096,7168;1024,4096,7168'")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3   # at least three untimed warm-up steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    dist_on = world > 1
+    if dist_on:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        torch.distributed.init_process_group("nccl")
+    run_ours(args, dist_on, rank, world)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
