@@ -60,7 +60,7 @@ nvfp4_status_t run(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb,
   auto kern = bs_gemm_kernel<C, false>;
   nvfp4_status_t st = allow_smem(reinterpret_cast<const void *>(kern), C::smem_bytes(false), dev.device);
   if (st != NVFP4_OK) return st;
-  cudaError_t e = launch(kern, dim3(pl.ctas), dim3(192), C::smem_bytes(false), s,
+  cudaError_t e = launch(kern, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
                          (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, args);
   return check_launch(e, "nvfp4_gemm");
 }

@@ -5,17 +5,24 @@
 //   C[i, j] = sum_k deq(A)[i, k] * deq(B)[j, k]   (fp32 accumulation in tensor memory)
 //   D       = bf16(alpha * C)                     (alpha on the fp32 value, one conversion)
 // A and B are K-major packed e2m1 (two per byte); their scales (ue4m3 per 16 for NVFP4, ue8m0
-// per 32 for MXFP4) are in the 128x4 swizzled layout, whose 512-byte tiles are exactly the
-// 32-row x 16-byte blocks one tcgen05.cp 32x128b.warpx4 moves into tensor memory.
+// per 32 for MXFP4) are in the 128x4 swizzled layout.  The block-scaled MMA reads the scales of
+// the 128 rows of a 512-byte tile from 4 tensor-memory columns of each 32-lane quadrant: lane
+// 32q+i, column j holds the 4 bytes at tile offset 16*i + 4*j, the same in every quadrant.
 //
-// CTA = 6 warps:
+// CTA = 10 warps:
 //   warp 0      TMA producer: A/B tiles (128-byte swizzle) and scale chunks (bulk copies)
 //               into a STAGES-deep shared-memory ring, one mbarrier pair per stage;
-//   warp 1      allocates tensor memory; one lane copies the stage's scales to TMEM and issues
-//               4 MMAs (K = 64 each) per 256-wide K stage, then commits the stage back to the
-//               producer and, after the last K stage of a tile, the accumulator to the epilogue;
+//   warp 1      allocates tensor memory; one lane issues 4 MMAs (K = 64 each) per 256-wide K
+//               stage, then commits the stage back to the producer and the scale slot back to
+//               the scale writers, and after the last K stage of a tile the accumulator to the
+//               epilogue;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, alpha * acc in fp32, one RNE
-//               conversion to bf16, 256-bit stores.
+//               conversion to bf16, 256-bit stores;
+//   warps 6..9  scale writers: each reads the stage's scale tiles from shared memory and
+//               writes them into its own quadrant of a tensor-memory scale slot with
+//               tcgen05.st (SF_SLOTS slots in a ring), keeping those writes off the tensor pipe
+//               (a tcgen05.cp of one 512-byte tile occupies the pipe about as long as 40 % of a
+//               128x256x64 MMA).
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
 // Tiles are walked persistently (grid <= SM count).  With splits > 1, the CTAs of a
 // (splits, 1, 1) cluster each take a slice of K for the same tile and reduce their fp32 partial
@@ -47,15 +54,17 @@ struct GemmCfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
   static constexpr int SFA_COLS = CHUNKS * 4;
   static constexpr int SFB_COLS = SFB_BLOCKS * CHUNKS * 4;
-  static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // two slots, alternating per K stage
+  static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // columns of one scale slot
   static constexpr int NACC = (2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
   static constexpr int SF_COL0 = NACC * BN;
-  static constexpr int TMEM_USED = SF_COL0 + 2 * SF_SLOT;
+  static constexpr int SF_SLOTS = (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
+  static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int RED_BYTES = BM * BN * 4;  // split-K partial tile (reuses the stage ring)
   static constexpr int MAX_EXPERTS = 1024;
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
-  static constexpr int CTRL_BYTES = 256;
+  static constexpr int CTRL_BYTES = 512;
+  static constexpr int THREADS = 320;
   // dynamic shared memory: alignment slack, stage ring, barriers, expert tables (grouped only)
   static constexpr int smem_bytes(bool grouped) {
     return 1024 + STAGES * STAGE_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
@@ -157,7 +166,7 @@ __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
 }
 
 template <class C, bool GROUPED>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -167,7 +176,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t *empty = full + C::STAGES;
   uint64_t *accf = empty + C::STAGES;
   uint64_t *acce = accf + 2;
-  uint64_t *drain = acce + 2;
+  uint64_t *sff = acce + 2;           // scale slot written (4 scale-writer warps arrive)
+  uint64_t *sfe = sff + 4;            // scale slot free (MMA commit)
+  uint64_t *drain = sfe + 4;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
@@ -185,6 +196,10 @@ __global__ void __launch_bounds__(192, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&accf[a]), 1);
       mbar_init(smem_u32(&acce[a]), 4);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(smem_u32(&sff[q]), 4);
+      mbar_init(smem_u32(&sfe[q]), 1);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -288,27 +303,20 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t it = 0;
       for (int tile = tile0; tile < total_tiles; tile += tile_step) {
         const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+        if (t.kt1 <= t.kt0) continue;  // no K work (never planned: splits <= K stages)
         if (!mbar_wait(smem_u32(&acce[acc]), acc_phase ^ 1, wc)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * C::BN;
         for (int kt = t.kt0; kt < t.kt1; ++kt, ++it) {
+          const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
           if (!mbar_wait(smem_u32(&full[stage]), phase, wc)) goto mma_done;
-          tc_fence_after();
           *consumed = *consumed + 1;
+          if (!mbar_wait(smem_u32(&sff[s_idx]), s_round & 1, wc)) goto mma_done;
+          tc_fence_after();
           const uint8_t *st = smem + stage * C::STAGE_BYTES;
-          const uint32_t a_s = smem_u32(st), b_s = smem_u32(st + C::A_BYTES);
-          const uint32_t sfa_s = smem_u32(st + C::A_BYTES + C::B_BYTES);
-          const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
-          const uint32_t slot = tmem + C::SF_COL0 + (it & 1) * C::SF_SLOT;
-          const int nch = stage_chunks<C>(p, kt);
-          for (int c = 0; c < nch; ++c) {
-            tc_cp_32x128b_x4(slot + 4 * c, sdesc_rows16(sfa_s + 512 * c));
-            for (int b = 0; b < t.sfb_blocks; ++b)
-              tc_cp_32x128b_x4(slot + C::SFA_COLS + c * 4 * C::SFB_BLOCKS + 4 * b,
-                               sdesc_rows16(sfb_s + (b * C::CHUNKS + c) * 512));
-          }
+          const uint32_t slot = tmem + C::SF_COL0 + s_idx * C::SF_SLOT;
           const int nmma = stage_mmas(p, kt);
-          const uint64_t adesc = sdesc_k_sw128(a_s), bdesc = sdesc_k_sw128(b_s);
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(st)), bdesc = sdesc_k_sw128(smem_u32(st + C::A_BYTES));
           for (int j = 0; j < nmma; ++j) {
             const uint32_t accumulate = (kt > t.kt0 || j > 0) ? 1u : 0u;
             if constexpr (C::MX) {
@@ -322,6 +330,7 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
           tc_commit(smem_u32(&empty[stage]));
+          tc_commit(smem_u32(&sfe[s_idx]));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
@@ -335,6 +344,56 @@ __global__ void __launch_bounds__(192, 1)
       }
     mma_done:;
     }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ scale writers
+    // Each warp fills its own 32-lane quadrant of the slot with the full scale data of the
+    // stage (the MMA reads every quadrant): lane i takes bytes 16*i .. 16*i+15 of every
+    // 512-byte scale tile, i.e. 4 consecutive columns per tile.
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t it = 0;
+    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+      if (t.kt1 <= t.kt0) continue;
+      for (int kt = t.kt0; kt < t.kt1; ++kt, ++it) {
+        const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
+        if (!mbar_wait(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc)) goto scale_done;
+        if (!mbar_wait(smem_u32(&full[stage]), phase, wc)) goto scale_done;
+        const uint32_t sfa_s = smem_u32(smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
+        const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
+        uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          const uint4 v = lds128(sfa_s + 512 * c + 16 * lane);
+          ra[4 * c] = v.x;
+          ra[4 * c + 1] = v.y;
+          ra[4 * c + 2] = v.z;
+          ra[4 * c + 3] = v.w;
+#pragma unroll
+          for (int b = 0; b < C::SFB_BLOCKS; ++b) {
+            const uint4 w = lds128(sfb_s + (b * C::CHUNKS + c) * 512 + 16 * lane);
+            const int o = c * 4 * C::SFB_BLOCKS + 4 * b;
+            rb[o] = w.x;
+            rb[o + 1] = w.y;
+            rb[o + 2] = w.z;
+            rb[o + 3] = w.w;
+          }
+        }
+        const uint32_t slot = tmem + lane_base + C::SF_COL0 + s_idx * C::SF_SLOT;
+        tmem_st_32x32b<C::SFA_COLS>(slot, ra);
+        tmem_st_32x32b<C::SFB_COLS>(slot + C::SFA_COLS, rb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sff[s_idx]));
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  scale_done:;
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();
@@ -345,6 +404,7 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t acc_phase = 0;
     for (int tile = tile0; tile < total_tiles; tile += tile_step) {
       const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+      if (t.kt1 <= t.kt0) continue;  // no K work (never planned), mirrors the MMA issuer
       if (!mbar_wait(smem_u32(&accf[acc]), acc_phase, wc)) break;
       tc_fence_after();
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
@@ -365,8 +425,8 @@ __global__ void __launch_bounds__(192, 1)
               uint32_t v[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                v[i] = pack_bf16x2(alpha * __uint_as_float(r[16 * h + 2 * i]),
-                                   alpha * __uint_as_float(r[16 * h + 2 * i + 1]));
+                v[i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[16 * h + 2 * i])),
+                                   __fmul_rn(alpha, __uint_as_float(r[16 * h + 2 * i + 1])));
               st_global_v8(out + 16 * h, v);
             }
           }
@@ -376,7 +436,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < 32; ++i) {
             const int j = 32 * c + i;
             if (j < t.cols) {
-              const float v = alpha * __uint_as_float(r[i]);
+              const float v = __fmul_rn(alpha, __uint_as_float(r[i]));
               p.d[(t.out_j0 + j) * p.ldd + t.out_i0 + row] = __float2bfloat16_rn(v);
             }
           }
@@ -417,24 +477,47 @@ __global__ void __launch_bounds__(192, 1)
 
   if constexpr (!GROUPED) {
     if (p.splits > 1) {
-      // Split-K reduction across the cluster: CTA `rank` owns columns [c0, c1) of the tile.
+      // Split-K reduction across the cluster.  The partial tile is stored column-major
+      // (128 rows per column); CTA `rank` owns a contiguous 1/splits of its 4-row groups.  Each
+      // thread first issues the loads of every rank's partial (independent, so their latencies
+      // overlap), then sums them in rank order (fixed order: deterministic output).
       cluster_sync();
-      if (warp >= 2) {
-        const int row = threadIdx.x - 64;  // 0..127
+      if (warp >= 2 && warp < 6) {
+        const int tid = threadIdx.x - 64;  // 0..127
         const int rank = static_cast<int>(cluster_ctarank());
         const TileInfo t = tile_info<C, GROUPED>(p, tb, tile0, split);
         const float alpha = p.alpha ? *p.alpha : 1.0f;
-        const int per = (C::BN + p.splits - 1) / p.splits;
-        const int c0 = rank * per, c1 = min(C::BN, c0 + per);
+        constexpr int UNITS = C::BN * 128 / 4;  // float4 groups in the tile
+        const int u0 = rank * UNITS / p.splits, u1 = (rank + 1) * UNITS / p.splits;
         const uint32_t red0 = smem_u32(smem);
-        for (int c = c0; c < c1; ++c) {
-          const uint32_t off = red0 + static_cast<uint32_t>((c * 128 + row) * 4);
-          float v = 0.0f;
-          for (int s = 0; s < p.splits; ++s) v += ld_cluster_f32(map_to_rank(off, s));
-          if (row < t.rows && c < t.cols) {
-            const __nv_bfloat16 b = __float2bfloat16_rn(alpha * v);
-            if (p.swap) p.d[(t.out_j0 + c) * p.ldd + t.out_i0 + row] = b;
-            else p.d[(t.out_i0 + row) * p.ldd + t.out_j0 + c] = b;
+        for (int u = u0 + tid; u < u1; u += 128) {
+          const uint32_t off = red0 + static_cast<uint32_t>(u * 16);
+          float4 part[8];
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            if (s < p.splits) part[s] = ld_cluster_v4(map_to_rank(off, s));
+          float4 v = part[0];
+#pragma unroll
+          for (int s = 1; s < 8; ++s)
+            if (s < p.splits) {
+              v.x += part[s].x;
+              v.y += part[s].y;
+              v.z += part[s].z;
+              v.w += part[s].w;
+            }
+          const int c = (u * 4) / 128, r0 = (u * 4) % 128;
+          if (r0 < t.rows && c < t.cols) {
+            const float o[4] = {v.x, v.y, v.z, v.w};
+            if (p.swap) {
+              uint2 pk;
+              pk.x = pack_bf16x2(__fmul_rn(alpha, o[0]), __fmul_rn(alpha, o[1]));
+              pk.y = pack_bf16x2(__fmul_rn(alpha, o[2]), __fmul_rn(alpha, o[3]));
+              *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                p.d[(t.out_i0 + r0 + i) * p.ldd + t.out_j0 + c] = __float2bfloat16_rn(__fmul_rn(alpha, o[i]));
+            }
           }
         }
       }
