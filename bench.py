@@ -24,13 +24,11 @@ second graph of the step's GEMM launches.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
-import math
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -61,6 +59,24 @@ def quant_bytes(m, k, vec=16):
     return 2 * m * k + m * k // 2 + m * k // vec
 
 
+def recorded_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the last ncu capture (profiles/gemm_traffic.json), or
+    None when the GEMM sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for src in rec["kernel_sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec["kernel_sha256"] or workload not in rec:
+        return None
+    return rec[workload]["dram_bytes_per_launch_avg"]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -71,50 +87,56 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi sampler (every 200 ms) around the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled every ~1 ms through NVML (read-only queries)
+    while the timed region runs; nvidia-smi (200 ms) if NVML cannot be loaded."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, device: int):
-        self.path = tempfile.mktemp(suffix=".csv")
-        args = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
-        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].strip()
-        self.index = vis if vis.isdigit() else None   # nvidia-smi index of the GPU in use
+        import threading
+        self.samples, self.mask, self.max_mhz, self.err = [], 0, None, None
+        self.stop_ev = threading.Event()
         try:
-            self.f = open(self.path, "w")
-            self.p = subprocess.Popen(args, stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.p = None
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            nv.nvmlInit_v2()
+            h = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                cnt = ctypes.c_uint()
+                nv.nvmlDeviceGetCount_v2(ctypes.byref(cnt))
+                if cnt.value != 1 or nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                    raise RuntimeError("NVML device not found")
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.nv, self.h = nv, h
+            self.t = threading.Thread(target=self._poll, daemon=True)
+            self.t.start()
+        except Exception as e:  # noqa: BLE001
+            self.err = f"NVML unavailable ({e})"
+            self.t = None
+
+    def _poll(self):
+        mhz, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_r = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_ev.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if get_r(self.h, ctypes.byref(reasons)) == 0:
+                self.mask |= reasons.value
+            time.sleep(0.001)
 
     def stop(self) -> dict:
-        if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.p.terminate()
-        self.p.wait()
-        self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            rows = [[x.strip() for x in line.split(",")] for line in f]
-        indices = sorted({r[0] for r in rows if len(r) >= 9})
-        want = self.index if self.index in indices else (indices[0] if indices else None)
-        for parts in rows:
-            if len(parts) < 9 or parts[0] != want:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if self.t is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.err]}
+        self.stop_ev.set()
+        self.t.join()
+        reasons = sorted(v for k, v in self.REASONS.items() if self.mask & k)
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "source": "NVML, 1 ms polling during the timed steps"}
 
 
 # ---------------------------------------------------------------------------- workloads
@@ -332,7 +354,7 @@ def run_ours(args, dist_on, rank, world):
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist_on)
 
     # ---- GEMM kernels alone (roofline of the dominant kernel)
-    gemm_ms = timed_replays(gemm_graph, max(3, args.steps), flush)
+    gemm_ms = timed_replays(gemm_graph, max(3, min(args.steps, 50)), flush)
     per_launch_ms = statistics.median(gemm_ms) / len(wl.gemm_launches)
     quant_ms = max(0.0, ms - statistics.median(gemm_ms))
 
@@ -345,7 +367,7 @@ def run_ours(args, dist_on, rank, world):
         for host_t, dev_t in wl.d2h:
             host_t.copy_(dev_t, non_blocking=True)
 
-    e2e_ms_list = timed_replays(step_graph, args.steps, flush, before=h2d, after=d2h)
+    e2e_ms_list = timed_replays(step_graph, max(3, min(args.steps, 50)), flush, before=h2d, after=d2h)
     e2e_ms = max_over_ranks(statistics.mean(e2e_ms_list), dist_on)
     h2d_bytes = sum(t.numel() * t.element_size() for _, t in wl.h2d)
     d2h_bytes = sum(t.numel() * t.element_size() for t, _ in wl.d2h)
@@ -359,8 +381,10 @@ def run_ours(args, dist_on, rank, world):
     t_roof = max(wl.flops / (fp4_peak_tflops * 1e12), wl.gemm_bytes / (hbm * 1e9))
     bound = "hbm" if wl.gemm_bytes / (hbm * 1e9) >= wl.flops / (fp4_peak_tflops * 1e12) else "tensor"
     if bound == "hbm":
+        tr = recorded_traffic(wl.name)
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(gemm_gbs / hbm, 4), "traffic": None}
+                "frac": round(gemm_gbs / hbm, 4), "traffic": None if tr is None else round(tr),
+                "algorithmic_bytes_per_launch": round(wl.gemm_bytes / len(wl.gemm_launches))}
     else:
         roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak_tflops, 1),
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak_tflops, 4), "traffic": None}
@@ -471,7 +495,7 @@ def run_reference(args, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(MAKERS), default="decode")

@@ -67,7 +67,14 @@ enum {
   NVFP4_FLAG_PDL = 1u << 0,
   /* Short (about 20 ms) limit on every pipeline wait instead of the default (about 10 s);
    * for tests of the timeout path. */
-  NVFP4_FLAG_DEBUG_TIMEOUT = 1u << 8
+  NVFP4_FLAG_DEBUG_TIMEOUT = 1u << 8,
+  /* Test hook of the time-out path (GEMMs only, honoured only together with
+   * NVFP4_FLAG_DEBUG_TIMEOUT): the loader posts the byte count of the first K stage of each CTA
+   * but issues none of its copies, so the wait for that stage runs out.  The kernel then records
+   * the time-out (nvfp4_check_status returns NVFP4_ERR_TIMEOUT), drains its bounded waits, frees
+   * its tensor memory and exits; the output is undefined.  Nothing is read or written out of
+   * bounds. */
+  NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD = 1u << 9
 };
 
 /* Message for the last error on the calling thread ("" when the last call succeeded). */

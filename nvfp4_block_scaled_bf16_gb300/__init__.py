@@ -22,6 +22,7 @@ _i64, _u32, _int, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int, ctyp
 
 FLAG_PDL = 1 << 0
 FLAG_DEBUG_TIMEOUT = 1 << 8
+FLAG_DEBUG_SKIP_FIRST_LOAD = 1 << 9
 
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_MISALIGNED",
           3: "NVFP4_ERR_UNSUPPORTED_SHAPE", 4: "NVFP4_ERR_UNSUPPORTED_DEVICE", 5: "NVFP4_ERR_CUDA",

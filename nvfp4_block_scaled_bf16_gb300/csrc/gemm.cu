@@ -96,7 +96,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: m=%lld n=%lld k=%lld", (long long)m, (long long)n, (long long)k);
   if (k % 32 || n % 32)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_gemm: need k %% 32 == 0 and n %% 32 == 0 (k=%lld n=%lld)", (long long)k, (long long)n);
-  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT))
+  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD))
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: unknown flags 0x%x", flags);
   if (m == 0) return NVFP4_OK;
   if (!a || !sfa || !b || !sfb || !alpha || !d) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: null pointer");
@@ -134,6 +134,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.sf_chunks = static_cast<int>(round_up(k / 16, 4) / 4);
   args.status = dev.status;
   args.wait_limit = wait_limit(flags);
+  args.debug_skip_first_load = (flags & NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD) && (flags & NVFP4_FLAG_DEBUG_TIMEOUT);
 
   cudaStream_t s = (cudaStream_t)stream;
   switch (pl.bn) {

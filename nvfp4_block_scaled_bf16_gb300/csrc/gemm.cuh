@@ -91,6 +91,7 @@ struct GemmArgs {
   int64_t sfb_expert_bytes;    // grouped: bytes of one expert's B scales
   unsigned int *status;
   long long wait_limit;
+  int debug_skip_first_load;  // test hook of the time-out path (see NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD)
 };
 
 struct TileInfo {
@@ -259,36 +260,52 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      pdl_wait();
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      for (int tile = tile0; tile < total_tiles; tile += tile_step) {
-        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
-        for (int kt = t.kt0; kt < t.kt1; ++kt) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc)) goto producer_done;
-          const int nch = stage_chunks<C>(p, kt);
-          const uint32_t bytes = C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks);
-          uint8_t *st = smem + stage * C::STAGE_BYTES;
-          const uint32_t bar = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(bar, bytes);
-          tma_load_2d(smem_u32(st), &tmA, bar, kt * 128, t.a_y);
-          tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, bar, kt * 128, t.b_y);
-          uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
-          bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
-          for (int b = 0; b < t.sfb_blocks; ++b)
-            bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
-                      t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512,
-                      nch * 512, bar);
-          ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
+    // Lane 0 keeps the ring bookkeeping and posts each stage's byte count; then lane 0 issues
+    // the A tile, lane 1 the B tile, lane 2 A's scales and lanes 3.. B's scale blocks, so the
+    // copies of a stage go out in parallel.  (Issuing the weight half, or L2 prefetches of it,
+    // ahead of the activation half was measured slower: every copy of an SM goes through one
+    // TMA queue, so anything queued first delays the stage the MMA needs next.)
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    auto issue = [&](const TileInfo &t, int kt, int stg) {
+      const int nch = stage_chunks<C>(p, kt);
+      uint8_t *st = smem + stg * C::STAGE_BYTES;
+      const uint32_t bar = smem_u32(&full[stg]);
+      uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
+      if (lane == 0) tma_load_2d(smem_u32(st), &tmA, bar, kt * 128, t.a_y);
+      if (lane == 1) tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, bar, kt * 128, t.b_y);
+      if (lane == 2)
+        bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
+      if (lane >= 3 && lane < 3 + t.sfb_blocks) {
+        const int b = lane - 3;
+        bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
+                  t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+      }
+    };
+    pdl_wait();
+    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
+      for (int kt = t.kt0; kt < t.kt1; ++kt) {
+        int ok = 1;
+        if (lane == 0) {
+          ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc) ? 1 : 0;
+          if (ok) {
+            const int nch = stage_chunks<C>(p, kt);
+            mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
           }
         }
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto producer_done;
+        if (!(p.debug_skip_first_load && issued == 0)) issue(t, kt, stage);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
       }
-    producer_done:
+    }
+  producer_done:
+    if (lane == 0) {
       pdl_trigger();
       // remember how many stages were issued for the abort drain
       reinterpret_cast<volatile int *>(tmem_holder)[3] = issued;

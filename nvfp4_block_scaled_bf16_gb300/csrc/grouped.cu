@@ -31,7 +31,7 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
     return fail(NVFP4_ERR_INVALID_ARG, "mxfp4_grouped_gemm: experts * n too large");
   if (k % 32 || n % 32)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "mxfp4_grouped_gemm: need k %% 32 == 0 and n %% 32 == 0");
-  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT))
+  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD))
     return fail(NVFP4_ERR_INVALID_ARG, "mxfp4_grouped_gemm: unknown flags 0x%x", flags);
   if (t == 0) return NVFP4_OK;
   if (!a || !sfa || !row_offsets || !b || !sfb || !d) return fail(NVFP4_ERR_INVALID_ARG, "mxfp4_grouped_gemm: null pointer");
@@ -68,6 +68,7 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
   args.sfb_expert_bytes = static_cast<int64_t>(nvfp4_sf_bytes(n, k, 32));
   args.status = dev.status;
   args.wait_limit = wait_limit(flags);
+  args.debug_skip_first_load = (flags & NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD) && (flags & NVFP4_FLAG_DEBUG_TIMEOUT);
 
   auto kern = bs_gemm_kernel<GroupedCfg, true>;
   st = allow_smem(reinterpret_cast<const void *>(kern), GroupedCfg::smem_bytes(true), dev.device);
