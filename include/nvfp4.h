@@ -154,6 +154,9 @@ nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b
                           uint32_t flags, nvfp4_stream_t stream);
 
 /* MXFP4 grouped (MoE) GEMM: for every expert e, D[rows of e, :] = alpha * deq(A_e) deq(B_e)^T.
+ * The kernel checks row_offsets on the device (row_offsets[0] == 0, row_offsets[E] == t,
+ * non-decreasing); if they are malformed it does no work and nvfp4_check_status reports
+ * NVFP4_ERR_INVALID_ARG.
  * Source: [vLLM-51158] "Changes" (CUTLASS MXFP4 grouped GEMM over experts; SM10x/SM12x share
  * the block-scaled scale layout) and [vLLM-SM103] ops.h (expert offsets as arguments).
  *   a            uint8 [t, k/2] (rows sorted by expert), 32-B aligned
@@ -181,8 +184,10 @@ nvfp4_status_t sf_swizzle(const uint8_t *src, uint8_t *dst, int64_t rows, int64_
                           int to_swizzled, nvfp4_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that kernels set when a
- * bounded pipeline wait gave up.  Returns NVFP4_ERR_TIMEOUT if any kernel timed out since the
- * last check, NVFP4_ERR_CUDA if the synchronisation failed, NVFP4_OK otherwise. */
+ * bounded pipeline wait gave up or a grouped GEMM found malformed row offsets.  Returns
+ * NVFP4_ERR_INVALID_ARG for malformed offsets (the kernel did no work), NVFP4_ERR_TIMEOUT if a
+ * kernel timed out since the last check, NVFP4_ERR_CUDA if the synchronisation failed,
+ * NVFP4_OK otherwise. */
 nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream);
 
 #ifdef __cplusplus

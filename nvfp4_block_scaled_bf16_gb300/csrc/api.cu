@@ -172,6 +172,8 @@ extern "C" nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream) {
   if (word) {
     const unsigned int zero = 0;
     cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (word & 2u)
+      return fail(NVFP4_ERR_INVALID_ARG, "a grouped kernel found malformed row offsets and did no work (status 0x%x)", word);
     return fail(NVFP4_ERR_TIMEOUT, "a kernel gave up a bounded pipeline wait (status 0x%x)", word);
   }
   return NVFP4_OK;

@@ -44,6 +44,8 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     const int tiles = pl.m_tiles * pl.n_tiles;
     pl.ctas = tiles < sm_count ? tiles : sm_count;
   }
+  // Rings as deep as shared memory allows: a swap-AB CTA then has its whole K slice in flight
+  // from the start (the decode GEMM is bound by load latency, not by shared memory).
   switch (pl.bn) {
     case 32: pl.stages = 8; break;
     case 64: pl.stages = 7; break;
@@ -53,10 +55,10 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   return pl;
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool MULTI_TILE>
 nvfp4_status_t run(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                    const DeviceInfo &dev, uint32_t flags, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES, false>;
+  using C = GemmCfg<BN, STAGES, false, MULTI_TILE>;
   auto kern = bs_gemm_kernel<C, false>;
   nvfp4_status_t st = allow_smem(reinterpret_cast<const void *>(kern), C::smem_bytes(false), dev.device);
   if (st != NVFP4_OK) return st;
@@ -127,6 +129,8 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.n = static_cast<int>(rows_b);
   args.k = static_cast<int>(k);
   args.swap = pl.swap;
+  // b (the weight) may be read before the PDL wait (header contract); only worth it under PDL
+  args.weight_operand = (flags & NVFP4_FLAG_PDL) ? (pl.swap ? 1 : 2) : 0;
   args.m_tiles = pl.m_tiles;
   args.n_tiles = pl.n_tiles;
   args.k_tiles = pl.k_tiles;
@@ -138,9 +142,12 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
 
   cudaStream_t s = (cudaStream_t)stream;
   switch (pl.bn) {
-    case 32: return run<32, 8>(pl, ta, tb, args, dev, flags, s);
-    case 64: return run<64, 7>(pl, ta, tb, args, dev, flags, s);
-    case 128: return run<128, 6>(pl, ta, tb, args, dev, flags, s);
-    default: return run<256, 4>(pl, ta, tb, args, dev, flags, s);
+    // swap-AB CTAs own one tile each (single accumulator); large-M CTAs walk tiles persistently
+    case 32: return run<32, 8, false>(pl, ta, tb, args, dev, flags, s);
+    case 64: return run<64, 7, false>(pl, ta, tb, args, dev, flags, s);
+    case 128:
+      return pl.swap ? run<128, 6, false>(pl, ta, tb, args, dev, flags, s) : run<128, 6, true>(pl, ta, tb, args, dev, flags, s);
+    default:
+      return pl.swap ? run<256, 4, false>(pl, ta, tb, args, dev, flags, s) : run<256, 4, true>(pl, ta, tb, args, dev, flags, s);
   }
 }

@@ -37,7 +37,7 @@
 
 namespace nvfp4 {
 
-template <int BN_, int STAGES_, bool MX_>
+template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true>
 struct GemmCfg {
   static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
   static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
@@ -55,7 +55,9 @@ struct GemmCfg {
   static constexpr int SFA_COLS = CHUNKS * 4;
   static constexpr int SFB_COLS = SFB_BLOCKS * CHUNKS * 4;
   static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // columns of one scale slot
-  static constexpr int NACC = (2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
+  // a second accumulator only helps CTAs that walk several tiles (epilogue of tile t overlaps
+  // the mainloop of t+1); single-tile CTAs keep tensor memory small enough for two per SM
+  static constexpr int NACC = (MULTI_TILE_ && 2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
   static constexpr int SF_COL0 = NACC * BN;
   static constexpr int SF_SLOTS = (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
@@ -84,6 +86,7 @@ struct GemmArgs {
   int64_t ldd;              // output row stride (elements)
   int m, n, k;              // operand A rows, operand B rows (per expert when grouped), K
   int swap;                 // 1: D[j][i] = C[i][j] (operand A is the weight)
+  int weight_operand;       // launched with PDL: 1 = A, 2 = B is the weight (loaded before the wait)
   int m_tiles, n_tiles, k_tiles, splits;
   int sf_chunks;            // 512-byte scale chunks per 128-row block = round_up(K/VEC, 4) / 4
   const int64_t *row_offsets;  // grouped: [experts + 1] rows of operand A per expert
@@ -92,6 +95,7 @@ struct GemmArgs {
   unsigned int *status;
   long long wait_limit;
   int debug_skip_first_load;  // test hook of the time-out path (see NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD)
+  int max_tiles;              // grouped: host bound of the work list, (ceil(t/128) + experts) * n_tiles
 };
 
 struct TileInfo {
@@ -166,6 +170,27 @@ __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
   return min(4, (p.k - kt * 256 + 63) / 64);
 }
 
+// Copies of K stage kt into ring slot stg, one per lane: lane 0 the A tile, lane 1 the B tile,
+// lane 2 A's scale chunks, lanes 3.. B's scale blocks (only the requested operand halves).
+template <class C>
+__device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t, int kt, int stg, uint8_t *smem,
+                                            uint64_t *full, const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                            int lane, bool do_a, bool do_b) {
+  const int nch = stage_chunks<C>(p, kt);
+  uint8_t *st = smem + stg * C::STAGE_BYTES;
+  const uint32_t bar = smem_u32(&full[stg]);
+  uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
+  if (do_a && lane == 0) tma_load_2d(smem_u32(st), tmA, bar, kt * 128, t.a_y);
+  if (do_b && lane == 1) tma_load_2d(smem_u32(st + C::A_BYTES), tmB, bar, kt * 128, t.b_y);
+  if (do_a && lane == 2)
+    bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
+  if (do_b && lane >= 3 && lane < 3 + t.sfb_blocks) {
+    const int b = lane - 3;
+    bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
+              t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+  }
+}
+
 template <class C, bool GROUPED>
 __global__ void __launch_bounds__(320, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -188,6 +213,9 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const WaitCtl wc{p.wait_limit, abort_flag, p.status};
+  // The next kernel may launch now: it waits (griddepcontrol.wait) for this grid to complete
+  // before it reads our output, and its CTAs can meanwhile take the SM space we leave free.
+  if (threadIdx.x == 0) pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -209,13 +237,19 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-    tmem_relinquish();
+  int total_tiles = 0;
+  int tile0 = 0, tile_step = 1, split = 0;
+  if constexpr (!GROUPED) {
+    total_tiles = p.m_tiles * p.n_tiles;
+    if (p.splits > 1) {
+      tile0 = blockIdx.x / p.splits;
+      split = blockIdx.x % p.splits;
+      tile_step = total_tiles;  // exactly one tile per CTA
+    } else {
+      tile0 = blockIdx.x;
+      tile_step = gridDim.x;
+    }
   }
-
-  int total_tiles;
-  int tile0, tile_step, split = 0;
   if constexpr (GROUPED) {
     // Row offsets are produced by earlier kernels: read them only after the PDL wait.
     pdl_wait();
@@ -223,80 +257,93 @@ __global__ void __launch_bounds__(320, 1)
     for (int e = threadIdx.x; e <= E; e += blockDim.x) tb.ro[e] = static_cast<int>(p.row_offsets[e]);
     __syncthreads();
     if (threadIdx.x == 0) {
+      // The offsets are caller data: they must start at 0, end at the row count and never
+      // decrease, otherwise tile addresses could leave the caller's buffers.  A malformed array
+      // sets bit 1 of the status word and the kernel does no work.
+      bool ok = tb.ro[0] == 0 && tb.ro[E] == p.m;
       int sfr = 0, tp = 0;
       for (int e = 0; e < E; ++e) {
         tb.sfr[e] = sfr;
         tb.tp[e] = tp;
-        int cnt = tb.ro[e + 1] - tb.ro[e];
-        cnt = cnt < 0 ? 0 : cnt;
-        sfr += (cnt + 127) / 128 * 128;
-        tp += (cnt + 127) / 128 * p.n_tiles;
+        const int cnt = tb.ro[e + 1] - tb.ro[e];
+        ok = ok && cnt >= 0;
+        sfr += (max(cnt, 0) + 127) / 128 * 128;
+        tp += (max(cnt, 0) + 127) / 128 * p.n_tiles;
+      }
+      if (!ok || tp > p.max_tiles) {
+        if (blockIdx.x == 0) atomicOr(p.status, 2u);
+        tp = 0;
       }
       tb.sfr[E] = sfr;
       tb.tp[E] = tp;
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
 
+  __syncthreads();  // barriers initialised (and expert tables written, grouped)
   if constexpr (GROUPED) {
     total_tiles = tb.tp[p.experts];
     tile0 = blockIdx.x;
     tile_step = gridDim.x;
-  } else {
-    if (p.splits > 1) {
-      total_tiles = p.m_tiles * p.n_tiles;
-      tile0 = blockIdx.x / p.splits;
-      split = blockIdx.x % p.splits;
-      tile_step = total_tiles;  // exactly one tile per CTA
-    } else {
-      total_tiles = p.m_tiles * p.n_tiles;
-      tile0 = blockIdx.x;
-      tile_step = gridDim.x;
+  }
+  // The loader (warp 0) starts right away; warp 1 allocates tensor memory meanwhile and a named
+  // barrier among warps 1..9 (the tensor-memory users) publishes its address.
+  uint32_t tmem = 0;
+  if (warp != 0) {
+    if (warp == 1) {
+      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+      tmem_relinquish();
     }
+    tc_fence_before();
+    named_barrier_sync(1, C::THREADS - 32);
+    tc_fence_after();
+    tmem = *tmem_holder;
   }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 keeps the ring bookkeeping and posts each stage's byte count; then lane 0 issues
-    // the A tile, lane 1 the B tile, lane 2 A's scales and lanes 3.. B's scale blocks, so the
-    // copies of a stage go out in parallel.  (Issuing the weight half, or L2 prefetches of it,
-    // ahead of the activation half was measured slower: every copy of an SM goes through one
-    // TMA queue, so anything queued first delays the stage the MMA needs next.)
+    // Lane 0 keeps the ring bookkeeping and posts each stage's byte count; lanes 0-4 then issue
+    // the stage's copies in parallel (issue_stage).
     int stage = 0;
     uint32_t phase = 0;
     int issued = 0;
-    auto issue = [&](const TileInfo &t, int kt, int stg) {
-      const int nch = stage_chunks<C>(p, kt);
-      uint8_t *st = smem + stg * C::STAGE_BYTES;
-      const uint32_t bar = smem_u32(&full[stg]);
-      uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
-      if (lane == 0) tma_load_2d(smem_u32(st), &tmA, bar, kt * 128, t.a_y);
-      if (lane == 1) tma_load_2d(smem_u32(st + C::A_BYTES), &tmB, bar, kt * 128, t.b_y);
-      if (lane == 2)
-        bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
-      if (lane >= 3 && lane < 3 + t.sfb_blocks) {
-        const int b = lane - 3;
-        bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
-                  t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+    const bool skip_first = p.debug_skip_first_load != 0;
+    // Under PDL (p.weight_operand != 0) the weight half of the first ring of stages goes out
+    // before griddepcontrol.wait, so it streams while the preceding kernel finishes; the
+    // activation half follows in the loop below.
+    int pre = 0;
+    const bool pre_a = p.weight_operand == 1, pre_b = p.weight_operand == 2;
+    if (!GROUPED && (pre_a || pre_b) && tile0 < total_tiles) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile0, split);
+      pre = min(C::STAGES, t.kt1 - t.kt0);
+      for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
+        const int kt = t.kt0 + i;
+        if (lane == 0) {
+          const int nch = stage_chunks<C>(p, kt);
+          mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+        }
+        __syncwarp();
+        if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, lane, pre_a, pre_b);
       }
-    };
+    }
     pdl_wait();
     for (int tile = tile0; tile < total_tiles; tile += tile_step) {
       const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
       for (int kt = t.kt0; kt < t.kt1; ++kt) {
-        int ok = 1;
-        if (lane == 0) {
-          ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc) ? 1 : 0;
-          if (ok) {
-            const int nch = stage_chunks<C>(p, kt);
-            mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+        const bool early_stage = tile == tile0 && kt - t.kt0 < pre;
+        if (!early_stage) {
+          int ok = 1;
+          if (lane == 0) {
+            ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc) ? 1 : 0;
+            if (ok) {
+              const int nch = stage_chunks<C>(p, kt);
+              mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+            }
           }
+          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto producer_done;
         }
-        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto producer_done;
-        if (!(p.debug_skip_first_load && issued == 0)) issue(t, kt, stage);
+        const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
+        if (!(skip_first && issued == 0) && (do_a || do_b))
+          issue_stage<C>(p, t, kt, stage, smem, full, &tmA, &tmB, lane, do_a, do_b);
         ++issued;
         if (++stage == C::STAGES) {
           stage = 0;
@@ -306,7 +353,6 @@ __global__ void __launch_bounds__(320, 1)
     }
   producer_done:
     if (lane == 0) {
-      pdl_trigger();
       // remember how many stages were issued for the abort drain
       reinterpret_cast<volatile int *>(tmem_holder)[3] = issued;
     }
@@ -469,6 +515,7 @@ __global__ void __launch_bounds__(320, 1)
     }
   }
 
+  tc_fence_before();  // order this warp's tcgen05 work before the barrier (dealloc follows it)
   __syncthreads();
   if (*abort_flag) {
     // Drain: wait (bounded) for copies still landing in shared memory and for outstanding

@@ -70,6 +70,9 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
   args.wait_limit = wait_limit(flags);
   args.debug_skip_first_load = (flags & NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD) && (flags & NVFP4_FLAG_DEBUG_TIMEOUT);
 
+  const int64_t bound = (ceil_div(t, 128) + num_experts) * args.n_tiles;
+  if (bound >= (1LL << 31)) return fail(NVFP4_ERR_INVALID_ARG, "mxfp4_grouped_gemm: problem too large");
+  args.max_tiles = static_cast<int>(bound);
   auto kern = bs_gemm_kernel<GroupedCfg, true>;
   st = allow_smem(reinterpret_cast<const void *>(kern), GroupedCfg::smem_bytes(true), dev.device);
   if (st != NVFP4_OK) return st;

@@ -47,8 +47,10 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *_
                                                           uint8_t *__restrict__ q,
                                                           uint8_t *__restrict__ sf, int64_t total,
                                                           int64_t cp) {
-  pdl_wait();
+  // Let the next kernel launch at once (it waits for this grid's completion before it reads
+  // our outputs), then wait for our own predecessor before reading x.
   pdl_trigger();
+  pdl_wait();
   const float gs = __ldg(gs_ptr);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -96,8 +98,10 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
                                                           int64_t cap_rows, int64_t cp) {
   __shared__ int64_t s_ro[kMaxExperts + 1];
   __shared__ int64_t s_sfr[kMaxExperts + 1];
-  pdl_wait();
+  // Let the next kernel launch at once (it waits for this grid's completion before it reads
+  // our outputs), then wait for our own predecessor before reading x.
   pdl_trigger();
+  pdl_wait();
   if (row_offsets == nullptr) {
     if (threadIdx.x == 0) {
       s_ro[0] = 0;

@@ -70,3 +70,21 @@ def test_moe_gate_up_sampled_experts(nv):
     rng = np.random.default_rng(0)
     pick = sorted(set([int(order[0]), int(order[-1])] + [int(v) for v in rng.integers(0, 128, 6)]))
     _check(nv, counts, 1536, 2048, experts_to_check=pick)
+
+
+def test_malformed_row_offsets_are_rejected_on_device(nv):
+    """Offsets that do not end at the row count (or decrease) make the kernel do no work and
+    nvfp4_check_status report NVFP4_ERR_INVALID_ARG; the output is left untouched."""
+    E, n, k, t = 3, 128, 256, 64
+    qa = torch.zeros((t, k // 2), dtype=torch.uint8, device="cuda")
+    sfa = torch.zeros(nv.grouped_sf_bytes(t, E, k), dtype=torch.uint8, device="cuda")
+    qb = torch.zeros((E, n, k // 2), dtype=torch.uint8, device="cuda")
+    sfb = torch.zeros((E, nv.sf_bytes(n, k, 32)), dtype=torch.uint8, device="cuda")
+    for bad in ([0, 10, 5, 64], [0, 10, 20, 60], [3, 10, 20, 64]):
+        d = torch.full((t, n), 7.0, dtype=torch.bfloat16, device="cuda")
+        nv.check_status()
+        nv.mxfp4_grouped_gemm(qa, sfa, torch.tensor(bad, device="cuda"), qb, sfb, None, d)
+        with pytest.raises(nv.NVFP4Error) as e:
+            nv.check_status()
+        assert e.value.code == 1
+        assert bool((d == 7.0).all())
