@@ -167,6 +167,8 @@ def _gs(x: torch.Tensor) -> float:
 def build_nvfp4_chain(nv, wl: Workload, shapes, weight_seed=0, weights_by_shape=None, pdl=True):
     flags = nv.FLAG_PDL if pdl else 0
     cache = {}
+    # one zeroed split-K workspace serves every GEMM of the chain (they run in stream order)
+    ws = nv.gemm_workspace(max(nv.gemm_workspace_size(m, n, k) for (m, n, k) in shapes))
     for i, (m, n, k) in enumerate(shapes):
         key = (n, k)
         if key not in cache:
@@ -185,7 +187,8 @@ def build_nvfp4_chain(nv, wl: Workload, shapes, weight_seed=0, weights_by_shape=
         sf = torch.empty(nv.sf_bytes(m, k), dtype=torch.uint8, device="cuda")
         d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
         wl.launches.append(lambda xd=xd, gs_d=gs_d, q=q, sf=sf: nv.nvfp4_quantize(xd, gs_d, q, sf, flags=flags))
-        g = (lambda q=q, sf=sf, qb=qb, sfb=sfb, al_d=al_d, d=d, f=flags: nv.nvfp4_gemm(q, sf, qb, sfb, al_d, d, flags=f))
+        g = (lambda q=q, sf=sf, qb=qb, sfb=sfb, al_d=al_d, d=d, f=flags:
+             nv.nvfp4_gemm(q, sf, qb, sfb, al_d, d, flags=f, workspace=ws))
         wl.launches.append(g)
         wl.gemm_launches.append(g)
         wl.flops += 2.0 * m * n * k

@@ -134,8 +134,17 @@ typedef struct {
   int splits;    /* K splits reduced inside a thread-block cluster (1 = none) */
   int stages;    /* shared-memory pipeline depth */
   int ctas;      /* CTAs launched */
+  int dp_tiles;  /* output tiles each computed whole by one CTA */
+  int sk_tiles;  /* output tiles after those whose K stages are split stream-K over all CTAs */
 } nvfp4_gemm_plan_t;
 nvfp4_status_t nvfp4_gemm_plan(int64_t m, int64_t n, int64_t k, nvfp4_gemm_plan_t *plan);
+
+/* Bytes of device workspace nvfp4_gemm needs for this shape on the current device (0 when the
+ * plan splits no tile).  Host only.  The split-K reduction is the library's own design (the
+ * pages' kernels pick split-K for small M but do not describe how partials are added): the
+ * workspace holds one arrival counter per split tile followed by two fp32 partial-tile slots
+ * of 128 x tile_n per CTA. */
+nvfp4_status_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes);
 
 /* NVFP4 block-scaled GEMM with bf16 output.
  * Source: [vLLM-SM103] nvfp4_scaled_mm_kernels.cu "SM103 Entry Point" (A [M,K/2] packed e2m1
@@ -147,11 +156,20 @@ nvfp4_status_t nvfp4_gemm_plan(int64_t m, int64_t n, int64_t k, nvfp4_gemm_plan_
  *   a      uint8 [m, k/2], 32-B aligned         sfa  nvfp4_sf_bytes(m,k,16) bytes, 16-B aligned
  *   b      uint8 [n, k/2], 32-B aligned         sfb  nvfp4_sf_bytes(n,k,16) bytes, 16-B aligned
  *   alpha  device fp32 scalar, 4-B aligned       d    bf16 [m, n] row-major, 32-B aligned
+ *   workspace    device buffer of at least nvfp4_gemm_workspace_size(m,n,k) bytes, 256-B
+ *                aligned (may be NULL when that size is 0).  It must be zero-filled before its
+ *                first use; every call that completes leaves it zero again, so one zeroing
+ *                serves any number of calls.  Calls that can run at the same time (other
+ *                streams) need separate workspaces: the kernel's counters and partial tiles
+ *                would race.  After a call that reported NVFP4_ERR_TIMEOUT, zero it again.
  *   n % 32 == 0, k % 32 == 0, m, n, k < 2^31.
- * With NVFP4_FLAG_PDL, b and sfb may be read before the wait for the preceding kernel. */
+ * The output does not depend on timing: split tiles are added in a fixed order.
+ * With NVFP4_FLAG_PDL, b and sfb may be read before the wait for the preceding kernel; the
+ * workspace is touched only after that wait. */
 nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb,
                           const float *alpha, void *d, int64_t m, int64_t n, int64_t k,
-                          uint32_t flags, nvfp4_stream_t stream);
+                          void *workspace, size_t workspace_bytes, uint32_t flags,
+                          nvfp4_stream_t stream);
 
 /* MXFP4 grouped (MoE) GEMM: for every expert e, D[rows of e, :] = alpha * deq(A_e) deq(B_e)^T.
  * The kernel checks row_offsets on the device (row_offsets[0] == 0, row_offsets[E] == t,

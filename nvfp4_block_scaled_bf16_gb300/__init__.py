@@ -31,7 +31,7 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_MISALIGNED",
 
 class PlanT(ctypes.Structure):
     _fields_ = [("swap_ab", _int), ("tile_m", _int), ("tile_n", _int), ("splits", _int),
-                ("stages", _int), ("ctas", _int)]
+                ("stages", _int), ("ctas", _int), ("dp_tiles", _int), ("sk_tiles", _int)]
 
 
 _SIGS = {
@@ -41,7 +41,8 @@ _SIGS = {
     "nvfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _u32, _vp]),
     "mxfp4_quantize": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u32, _vp]),
     "nvfp4_gemm_plan": (_int, [_i64, _i64, _i64, ctypes.POINTER(PlanT)]),
-    "nvfp4_gemm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
+    "nvfp4_gemm_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
+    "nvfp4_gemm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_check_status": (_int, [_vp]),
@@ -106,6 +107,31 @@ def nvfp4_gemm_plan(m: int, n: int, k: int) -> dict:
     return {f: getattr(p, f) for f, _ in PlanT._fields_}
 
 
+def gemm_workspace_size(m: int, n: int, k: int) -> int:
+    """Bytes of workspace nvfp4_gemm needs for (m, n, k) on the current device."""
+    v = _sz(0)
+    _check(_lib.nvfp4_gemm_workspace_size(m, n, k, ctypes.byref(v)))
+    return int(v.value)
+
+
+def gemm_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled uint8 workspace of at least nbytes (the library needs it zero before first use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+_ws_cache: dict = {}
+
+
+def _default_workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """One zeroed workspace per device, grown on demand and shared by every nvfp4_gemm call that
+    passes none.  Calls on streams that may overlap must pass their own workspace."""
+    ws = _ws_cache.get(device)
+    if ws is None or ws.numel() < nbytes:
+        ws = gemm_workspace(nbytes, device)
+        _ws_cache[device] = ws
+    return ws
+
+
 def nvfp4_quantize(x, gs, q=None, sf=None, flags: int = 0, stream=None):
     """bf16 [m, k] -> (packed e2m1 uint8 [m, k/2], swizzled e4m3 scales uint8 [sf_bytes])."""
     _need(x, torch.bfloat16, "x", 2)
@@ -141,8 +167,11 @@ def mxfp4_quantize(x, row_offsets=None, q=None, sf=None, flags: int = 0, stream=
     return q, sf
 
 
-def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None):
-    """D[m, n] = bf16(alpha * deq(a) @ deq(b)^T); a [m, k/2], b [n, k/2] packed uint8."""
+def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None, workspace=None):
+    """D[m, n] = bf16(alpha * deq(a) @ deq(b)^T); a [m, k/2], b [n, k/2] packed uint8.
+
+    workspace: zero-filled uint8 CUDA tensor of at least gemm_workspace_size(m, n, k) bytes
+    (the library leaves it zero after each call); None uses a per-device shared one."""
     _need(a, torch.uint8, "a", 2)
     _need(b, torch.uint8, "b", 2)
     _need(sfa, torch.uint8, "sfa")
@@ -159,7 +188,14 @@ def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None):
         raise ValueError("scale buffers are too small")
     if d is None:
         d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
-    _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh, flags,
+    if workspace is None and m > 0:
+        need = gemm_workspace_size(m, n, 2 * kh)
+        if need:
+            workspace = _default_workspace(need, a.device)
+    if workspace is not None:
+        _need(workspace, torch.uint8, "workspace")
+    _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
+                           _ptr(workspace), 0 if workspace is None else workspace.numel(), flags,
                            _stream(stream)))
     return d
 

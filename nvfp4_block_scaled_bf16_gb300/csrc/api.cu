@@ -174,7 +174,17 @@ extern "C" nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream) {
     cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (word & 2u)
       return fail(NVFP4_ERR_INVALID_ARG, "a grouped kernel found malformed row offsets and did no work (status 0x%x)", word);
-    return fail(NVFP4_ERR_TIMEOUT, "a kernel gave up a bounded pipeline wait (status 0x%x)", word);
+    if (word & 4u)
+      return fail(NVFP4_ERR_CUDA, "internal: a split tile had more partials than the fix-up buffer holds (status 0x%x)", word);
+    static const char *const kSites[7] = {"load/free-slot", "mma/accumulator", "mma/stage", "mma/scales",
+                                          "scales/slot", "scales/stage", "epilogue/accumulator"};
+    char sites[160] = "";
+    for (int i = 0; i < 7; ++i)
+      if (word & (1u << (8 + i))) {
+        strncat(sites, sites[0] ? ", " : "", sizeof(sites) - strlen(sites) - 1);
+        strncat(sites, kSites[i], sizeof(sites) - strlen(sites) - 1);
+      }
+    return fail(NVFP4_ERR_TIMEOUT, "a kernel gave up a bounded pipeline wait (status 0x%x; waits: %s)", word, sites);
   }
   return NVFP4_OK;
 }

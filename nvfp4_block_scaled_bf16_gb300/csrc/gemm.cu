@@ -8,9 +8,16 @@
 //             wasted on padding; K is split over a thread-block cluster of up to 8 CTAs until the
 //             grid covers the SMs, and the partial tiles are reduced through distributed
 //             shared memory (decode shapes are weight-streaming, so every SM must pull).
-//   M >  256  128 x 256 tiles (128 x 128 when N is not a multiple of 256... or fewer tiles
-//             than SMs), persistent over the SMs, double-buffered accumulators where tensor
-//             memory allows.
+//             Measured against a stream-K split through the workspace, the cluster reduction
+//             was 2 us faster at M <= 32 and 2x faster at M = 256, where one CTA would have to
+//             read every 128 KB partial of a tile.
+//   M >  256  128 x 256 tiles (128 x 128 when N is not a multiple of 256 or there are fewer
+//             256-wide tiles than SMs), persistent over the SMs, double-buffered accumulators
+//             where tensor memory allows.  When the tiles fill less than half the SMs and K is
+//             long (>= 4 K stages per SM), the (tile, K stage) units are split stream-K over all
+//             SMs and split tiles are added up through the workspace.  Splitting the last wave of
+//             large shapes the same way was measured slower: every SM is already bound by its
+//             own L2 -> shared-memory bandwidth, and the partials add traffic.
 #include "gemm.cuh"
 #include "host.h"
 
@@ -18,12 +25,30 @@ namespace nvfp4 {
 namespace {
 
 struct Plan {
-  int swap, bn, splits, stages, ctas, m_tiles, n_tiles, k_tiles;
+  int swap, bn, splits, stages, ctas, m_tiles, n_tiles, k_tiles, dp_tiles, sk_tiles;
+  size_t ws_bytes;
 };
+
+constexpr size_t kWsAlign = 256;
+
+// Most CTAs sharing one stream-K tile: the fix-up stages n 16 KB column chunks in the ring.
+constexpr int kMaxContributors = 12;
+
+int max_contributors(int64_t sk_tiles, int k_tiles, int ctas) {
+  const int64_t units = sk_tiles * k_tiles;
+  auto owner = [&](int64_t v) { return ((v + 1) * ctas + units - 1) / units - 1; };
+  int64_t most = 1;
+  for (int64_t t = 0; t < sk_tiles; ++t) {
+    const int64_t c = owner((t + 1) * k_tiles - 1) - owner(t * k_tiles) + 1;
+    most = c > most ? c : most;
+  }
+  return static_cast<int>(most);
+}
 
 Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   Plan pl{};
   pl.k_tiles = static_cast<int>(ceil_div(k, 256));
+  pl.splits = 1;
   if (m <= 256) {
     pl.swap = 1;
     pl.bn = m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
@@ -34,17 +59,34 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     s = s < 1 ? 1 : (s > 8 ? 8 : s);
     if (s > pl.k_tiles) s = pl.k_tiles;
     pl.splits = s;
+    pl.dp_tiles = tiles;
     pl.ctas = tiles * s;
   } else {
     pl.swap = 0;
     pl.bn = (n % 256 == 0 && ceil_div(m, 128) * (n / 256) >= sm_count) ? 256 : 128;
     pl.m_tiles = static_cast<int>(ceil_div(m, 128));
     pl.n_tiles = static_cast<int>(ceil_div(n, pl.bn));
-    pl.splits = 1;
     const int tiles = pl.m_tiles * pl.n_tiles;
+    const int64_t units = static_cast<int64_t>(tiles) * pl.k_tiles;
+    if (2 * tiles <= sm_count && units >= 4LL * sm_count) {
+      // few tiles with a long K: whole tiles would leave most SMs idle
+      pl.sk_tiles = tiles;
+      pl.ctas = sm_count;
+    } else {
+      pl.dp_tiles = tiles;
+      pl.ctas = tiles < sm_count ? tiles : sm_count;
+    }
+  }
+  if (pl.sk_tiles > 0 && max_contributors(pl.sk_tiles, pl.k_tiles, pl.ctas) > kMaxContributors) {
+    const int tiles = pl.dp_tiles + pl.sk_tiles;  // too fine a split: whole tiles instead
+    pl.dp_tiles = tiles;
+    pl.sk_tiles = 0;
     pl.ctas = tiles < sm_count ? tiles : sm_count;
   }
-  // Rings as deep as shared memory allows: a swap-AB CTA then has its whole K slice in flight
+  if (pl.sk_tiles > 0)
+    pl.ws_bytes = round_up(static_cast<int64_t>(pl.sk_tiles) * 4, kWsAlign) +
+                  static_cast<size_t>(pl.ctas) * 2 * 128 * pl.bn * 4;
+  // Rings as deep as shared memory allows: a swap-AB CTA then has its whole K run in flight
   // from the start (the decode GEMM is bound by load latency, not by shared memory).
   switch (pl.bn) {
     case 32: pl.stages = 8; break;
@@ -55,16 +97,32 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   return pl;
 }
 
-template <int BN, int STAGES, bool MULTI_TILE>
-nvfp4_status_t run(const Plan &pl, const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
-                   const DeviceInfo &dev, uint32_t flags, cudaStream_t s) {
-  using C = GemmCfg<BN, STAGES, false, MULTI_TILE>;
-  auto kern = bs_gemm_kernel<C, false>;
-  nvfp4_status_t st = allow_smem(reinterpret_cast<const void *>(kern), C::smem_bytes(false), dev.device);
-  if (st != NVFP4_OK) return st;
-  cudaError_t e = launch(kern, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
-                         (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, args);
-  return check_launch(e, "nvfp4_gemm");
+int plan_sm_count() {
+  int sms = 152;
+  DeviceInfo dev;
+  int cur = -1;
+  if (cudaGetDevice(&cur) == cudaSuccess && current_device(&dev) == NVFP4_OK) sms = dev.sm_count;
+  clear_error();
+  return sms;
+}
+
+// Calls f with the kernel configuration of a plan (a GemmCfg value).
+template <class F>
+nvfp4_status_t with_config(const Plan &pl, F &&f) {
+  // swap-AB CTAs hold one tile (single accumulator); large-M CTAs walk tiles persistently and
+  // overlap the epilogue with the next tile where tensor memory allows
+  switch (pl.bn) {
+    case 32: return f(GemmCfg<32, 8, false, false>{});
+    case 64: return f(GemmCfg<64, 7, false, false>{});
+    case 128: return pl.swap ? f(GemmCfg<128, 6, false, false>{}) : f(GemmCfg<128, 6, false, true>{});
+    default: return pl.swap ? f(GemmCfg<256, 4, false, false>{}) : f(GemmCfg<256, 4, false, true>{});
+  }
+}
+
+// Raises the kernel's dynamic shared-memory limit (once per kernel and device).
+template <class C>
+nvfp4_status_t prepare(const DeviceInfo &dev) {
+  return allow_smem(reinterpret_cast<const void *>(bs_gemm_kernel<C, false>), C::smem_bytes(false), dev.device);
 }
 
 }  // namespace
@@ -75,24 +133,29 @@ using namespace nvfp4;
 extern "C" nvfp4_status_t nvfp4_gemm_plan(int64_t m, int64_t n, int64_t k, nvfp4_gemm_plan_t *plan) {
   clear_error();
   if (!plan || m < 0 || n <= 0 || k <= 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm_plan: bad arguments");
-  int sms = 152;
-  DeviceInfo dev;
-  int cur = -1;
-  if (cudaGetDevice(&cur) == cudaSuccess && current_device(&dev) == NVFP4_OK) sms = dev.sm_count;
-  clear_error();
-  const Plan pl = select_plan(m, n, k, sms);
+  const Plan pl = select_plan(m, n, k, plan_sm_count());
   plan->swap_ab = pl.swap;
   plan->tile_m = 128;
   plan->tile_n = pl.bn;
   plan->splits = pl.splits;
   plan->stages = pl.stages;
   plan->ctas = pl.ctas;
+  plan->dp_tiles = pl.dp_tiles;
+  plan->sk_tiles = pl.sk_tiles;
+  return NVFP4_OK;
+}
+
+extern "C" nvfp4_status_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_t k, size_t *bytes) {
+  clear_error();
+  if (!bytes || m < 0 || n <= 0 || k <= 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm_workspace_size: bad arguments");
+  *bytes = m == 0 ? 0 : select_plan(m, n, k, plan_sm_count()).ws_bytes;
   return NVFP4_OK;
 }
 
 extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b,
                                      const uint8_t *sfb, const float *alpha, void *d, int64_t m,
-                                     int64_t n, int64_t k, uint32_t flags, nvfp4_stream_t stream) {
+                                     int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
+                                     uint32_t flags, nvfp4_stream_t stream) {
   clear_error();
   if (m < 0 || n <= 0 || k <= 0 || m >= (1LL << 31) || n >= (1LL << 31) || k >= (1LL << 31))
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: m=%lld n=%lld k=%lld", (long long)m, (long long)n, (long long)k);
@@ -109,6 +172,14 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   if (st != NVFP4_OK) return st;
 
   const Plan pl = select_plan(m, n, k, dev.sm_count);
+  st = with_config(pl, [&](auto cfg) { return prepare<decltype(cfg)>(dev); });
+  if (st != NVFP4_OK) return st;
+  if (pl.ws_bytes > 0) {
+    if (!workspace || workspace_bytes < pl.ws_bytes)
+      return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: this shape needs a workspace of %zu bytes (got %zu%s)",
+                  pl.ws_bytes, workspace_bytes, workspace ? "" : ", NULL");
+    if (!aligned(workspace, kWsAlign)) return fail(NVFP4_ERR_MISALIGNED, "nvfp4_gemm: workspace needs 256-B alignment");
+  }
   // Kernel operand A fills the 128-row MMA slot; with swap it is the weight B.
   const uint8_t *opa = pl.swap ? b : a, *opb = pl.swap ? a : b;
   const uint8_t *sfopa = pl.swap ? sfb : sfa, *sfopb = pl.swap ? sfa : sfb;
@@ -139,15 +210,19 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.status = dev.status;
   args.wait_limit = wait_limit(flags);
   args.debug_skip_first_load = (flags & NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD) && (flags & NVFP4_FLAG_DEBUG_TIMEOUT);
+  args.dp_tiles = pl.dp_tiles;
+  args.sk_tiles = pl.sk_tiles;
+  if (pl.sk_tiles > 0) {
+    args.ws_cnt = static_cast<unsigned int *>(workspace);
+    args.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                        round_up(static_cast<int64_t>(pl.sk_tiles) * 4, kWsAlign));
+  }
 
   cudaStream_t s = (cudaStream_t)stream;
-  switch (pl.bn) {
-    // swap-AB CTAs own one tile each (single accumulator); large-M CTAs walk tiles persistently
-    case 32: return run<32, 8, false>(pl, ta, tb, args, dev, flags, s);
-    case 64: return run<64, 7, false>(pl, ta, tb, args, dev, flags, s);
-    case 128:
-      return pl.swap ? run<128, 6, false>(pl, ta, tb, args, dev, flags, s) : run<128, 6, true>(pl, ta, tb, args, dev, flags, s);
-    default:
-      return pl.swap ? run<256, 4, false>(pl, ta, tb, args, dev, flags, s) : run<256, 4, true>(pl, ta, tb, args, dev, flags, s);
-  }
+  return with_config(pl, [&](auto cfg) {
+    using C = decltype(cfg);
+    const cudaError_t e = launch(bs_gemm_kernel<C, false>, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
+                                 (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, args);
+    return check_launch(e, "nvfp4_gemm");
+  });
 }

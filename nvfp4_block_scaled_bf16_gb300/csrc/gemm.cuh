@@ -24,9 +24,16 @@
 //               (a tcgen05.cp of one 512-byte tile occupies the pipe about as long as 40 % of a
 //               128x256x64 MMA).
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
-// Tiles are walked persistently (grid <= SM count).  With splits > 1, the CTAs of a
-// (splits, 1, 1) cluster each take a slice of K for the same tile and reduce their fp32 partial
-// tiles through distributed shared memory in a fixed order, so the result is deterministic.
+//
+// Work decomposition: each CTA walks a list of segments (tile, K-stage range).
+//   - whole tiles: CTA c takes tiles c, c+G, c+2G, ... below dp_tiles (G = grid size);
+//   - stream-K: the (tile, K stage) units of the sk_tiles tiles after them are cut into G
+//     contiguous runs of equal length, one per CTA.  A run that covers only part of a tile
+//     stores its fp32 partial tile in a workspace slot; the last CTA to finish the tile (an
+//     atomic counter per tile) adds the partials in contributor order -- a fixed order, so the
+//     result does not depend on timing -- and writes the bf16 output;
+//   - cluster split-K (splits > 1): the CTAs of a (splits, 1, 1) cluster each take a K slice of
+//     one tile and add their partials through distributed shared memory, also in a fixed order.
 //
 // Every mbarrier wait is bounded (WaitCtl).  When one gives up, the CTA records the time-out
 // in the device status word, every role leaves its loop, outstanding copies and MMAs are
@@ -36,6 +43,17 @@
 #include "ptx.cuh"
 
 namespace nvfp4 {
+
+// Wait sites recorded in the status word when a bounded wait gives up (bit 8 + site).
+enum : int {
+  kSiteLoadEmpty = 0,   // loader: free ring slot
+  kSiteMmaAcc = 1,      // MMA: accumulator drained by the epilogue
+  kSiteMmaFull = 2,     // MMA: stage landed
+  kSiteMmaScale = 3,    // MMA: scale slot written
+  kSiteScaleSlot = 4,   // scale writers: scale slot free
+  kSiteScaleFull = 5,   // scale writers: stage landed
+  kSiteEpilogue = 6     // epilogue: accumulator complete
+};
 
 template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true>
 struct GemmCfg {
@@ -62,7 +80,7 @@ struct GemmCfg {
   static constexpr int SF_SLOTS = (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int RED_BYTES = BM * BN * 4;  // split-K partial tile (reuses the stage ring)
+  static constexpr int RED_BYTES = BM * BN * 4;  // partial tile: cluster split-K buffer, stream-K slot
   static constexpr int MAX_EXPERTS = 1024;
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
   static constexpr int CTRL_BYTES = 512;
@@ -73,6 +91,7 @@ struct GemmCfg {
   }
   static constexpr uint32_t IDESC = idesc_block_scaled(BM, BN, MX, 0);
   static_assert(TMEM_USED <= 512, "tensor memory budget");
+  static_assert((2 * STAGES + 13) * 8 + 6 * 4 <= CTRL_BYTES, "barriers and flags fit the control block");
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(STAGE_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
@@ -96,6 +115,10 @@ struct GemmArgs {
   long long wait_limit;
   int debug_skip_first_load;  // test hook of the time-out path (see NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD)
   int max_tiles;              // grouped: host bound of the work list, (ceil(t/128) + experts) * n_tiles
+  int dp_tiles;               // tiles [0, dp_tiles) are computed whole
+  int sk_tiles;               // tiles [dp_tiles, dp_tiles + sk_tiles) are split stream-K
+  float *ws;                  // stream-K: 2 partial-tile slots (BM x BN fp32) per CTA
+  unsigned int *ws_cnt;       // stream-K: one arrival counter per split tile, zero between calls
 };
 
 struct TileInfo {
@@ -105,8 +128,77 @@ struct TileInfo {
   int sfb_blocks;              // B scale blocks present (<= SFB_BLOCKS)
   int rows, cols;              // valid rows of A / of B in this tile
   int64_t out_i0, out_j0;      // output coordinates of C[0][0] of the tile (before swap)
-  int kt0, kt1;                // K-stage range of this CTA
 };
+
+// One piece of a CTA's work: K stages [kt0, kt1) of tile `tile`.  n CTAs share the tile (n == 1:
+// this CTA computes it whole); this CTA is contributor j, counted from the one that holds K stage
+// 0, and c0 is the index of that first contributor (stream-K).
+struct Seg {
+  int tile, kt0, kt1, j, n, c0;
+};
+
+// Segment iterator.  Every role of the CTA walks the same sequence.
+struct Work {
+  int tile, tile_end, tile_step;  // whole tiles, or the one tile of a cluster split
+  int kt_lo, kt_hi, split, splits;
+  int64_t u, u_end, units;        // stream-K: this CTA's units [u, u_end) of `units`
+
+  // CTA whose run holds stream-K unit v: run c is [c*units/G, (c+1)*units/G)
+  __device__ __forceinline__ int owner(int64_t v) const {
+    return static_cast<int>(((v + 1) * gridDim.x + units - 1) / units - 1);
+  }
+  __device__ __forceinline__ bool next(const GemmArgs &p, Seg &s) {
+    if (tile < tile_end) {
+      s = Seg{tile, kt_lo, kt_hi, split, splits, 0};
+      tile += tile_step;
+      return true;
+    }
+    if (u < u_end) {
+      const int kt_n = p.k_tiles;
+      const int t = static_cast<int>(u / kt_n);
+      const int64_t first = static_cast<int64_t>(t) * kt_n;
+      const int kt0 = static_cast<int>(u - first);
+      const int kt1 = static_cast<int>(min(static_cast<int64_t>(kt_n), kt0 + (u_end - u)));
+      const int c0 = owner(first);
+      s = Seg{p.dp_tiles + t, kt0, kt1, static_cast<int>(blockIdx.x) - c0, owner(first + kt_n - 1) - c0 + 1, c0};
+      u += kt1 - kt0;
+      return true;
+    }
+    return false;
+  }
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ Work make_work(const GemmArgs &p, int grouped_tiles) {
+  Work w{};
+  w.kt_lo = 0;
+  w.kt_hi = p.k_tiles;
+  w.split = 0;
+  w.splits = 1;
+  w.u = w.u_end = 0;
+  w.units = 1;
+  w.tile = blockIdx.x;
+  w.tile_step = gridDim.x;
+  if (GROUPED) {
+    w.tile_end = grouped_tiles;
+  } else if (p.splits > 1) {
+    w.tile = blockIdx.x / p.splits;
+    w.tile_end = w.tile + 1;
+    w.tile_step = 1;
+    w.split = blockIdx.x % p.splits;
+    w.splits = p.splits;
+    w.kt_lo = static_cast<int>(static_cast<int64_t>(w.split) * p.k_tiles / p.splits);
+    w.kt_hi = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.k_tiles / p.splits);
+  } else {
+    w.tile_end = p.dp_tiles;
+    if (p.sk_tiles > 0) {
+      w.units = static_cast<int64_t>(p.sk_tiles) * p.k_tiles;
+      w.u = blockIdx.x * w.units / gridDim.x;
+      w.u_end = (blockIdx.x + 1) * w.units / gridDim.x;
+    }
+  }
+  return w;
+}
 
 template <class C, bool GROUPED>
 struct Tables {
@@ -116,8 +208,7 @@ struct Tables {
 };
 
 template <class C, bool GROUPED>
-__device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C, GROUPED> &tb,
-                                              int tile, int split) {
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C, GROUPED> &tb, int tile) {
   TileInfo t;
   int64_t sfb_base_block;
   if constexpr (GROUPED) {
@@ -141,8 +232,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C,
     t.cols = min(C::BN, p.n - nt * C::BN);
     t.out_i0 = t.a_y;
     t.out_j0 = nt * C::BN;
-    t.kt0 = 0;
-    t.kt1 = p.k_tiles;
   } else {
     const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
     t.a_y = mb * 128;
@@ -154,8 +243,6 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C,
     t.cols = min(C::BN, p.n - t.b_y);
     t.out_i0 = t.a_y;
     t.out_j0 = t.b_y;
-    t.kt0 = static_cast<int>(static_cast<int64_t>(split) * p.k_tiles / p.splits);
-    t.kt1 = static_cast<int>(static_cast<int64_t>(split + 1) * p.k_tiles / p.splits);
   }
   t.sfb_blocks = min(C::SFB_BLOCKS, (t.cols + 127) / 128);
   return t;
@@ -191,6 +278,84 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
   }
 }
 
+// Stream-K partial tiles.  A slot holds one CTA's fp32 partial of a 128 x BN tile in chunk-row
+// order: float (c*128 + r)*32 + i is row r, column 32c + i, i.e. what epilogue thread r reads
+// from tensor memory for chunk c, so the store is four full 32-byte sectors per thread and chunk.
+template <class C>
+__device__ __forceinline__ float *sk_slot(const GemmArgs &p, int cta, int j) {
+  return p.ws + static_cast<int64_t>(2 * cta + (j == 0 ? 1 : 0)) * (C::BM * C::BN);
+}
+
+// Fix-up of a split tile by the last CTA to finish it, run by the four epilogue warps (thread
+// tid = tile row) while the stage ring is idle:
+//   out = bf16(alpha * (P_0 + P_1 + ... + P_{n-1})), partials added in contributor order.
+// Columns are taken CW at a time: the n partials' chunks are copied into the ring with cp.async
+// (every copy in flight at once, 16-byte pieces XOR-swizzled by row so the row-wise reads hit
+// distinct banks), then each thread adds its row and writes 64 bytes of bf16 per chunk with
+// 256-bit stores.  The plan keeps n * 16 KB within the ring.
+template <class C>
+__device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, const Seg &s, float alpha, int tid,
+                                         uint8_t *smem) {
+  constexpr int RING = C::STAGES * C::STAGE_BYTES;
+  constexpr int CHUNK_BYTES = 128 * 32 * 4;  // one 32-column chunk of a partial
+  if (s.n * CHUNK_BYTES > RING) {  // never planned (the host caps contributors); uniform exit
+    if (tid == 0) atomicOr(p.status, 4u);
+    return;
+  }
+  int cw = C::BN;  // columns per pass, a power of two >= 32
+  while (cw > 32 && s.n * cw * 512 > RING) cw >>= 1;
+  const int chunks = cw / 32;
+  const uint32_t buf = smem_u32(smem);
+  const int row = tid;
+  fence_proxy_async_smem();  // the ring was last written by TMA and read by the tensor cores
+#pragma unroll 1
+  for (int c0 = 0; c0 < C::BN / 32; c0 += chunks) {
+#pragma unroll 1
+    for (int jj = 0; jj < s.n; ++jj) {
+      const float *src = sk_slot<C>(p, s.c0 + jj, jj) + static_cast<int64_t>(c0) * 128 * 32;
+#pragma unroll 1
+      for (int cc = 0; cc < chunks; ++cc) {
+        const uint32_t dst = buf + static_cast<uint32_t>((jj * chunks + cc) * CHUNK_BYTES);
+        const float *srcc = src + cc * 128 * 32;
+#pragma unroll
+        for (int e = tid; e < 1024; e += 128) {  // 1024 pieces of 16 bytes: row e/8, piece e%8
+          const int r = e >> 3, q = e & 7;
+          cp_async_16(dst + r * 128 + ((q ^ (r & 7)) << 4), srcc + e * 4);
+        }
+      }
+    }
+    cp_async_wait_all();
+    named_barrier_sync(2, 128);
+#pragma unroll 1
+    for (int cc = 0; cc < chunks; ++cc) {
+      const int c = c0 + cc;
+      if (row >= t.rows || 32 * c >= t.cols) continue;
+      float acc[32];
+#pragma unroll 1
+      for (int jj = 0; jj < s.n; ++jj) {
+        const uint32_t base = buf + static_cast<uint32_t>((jj * chunks + cc) * CHUNK_BYTES + row * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = lds128(base + ((q ^ (row & 7)) << 4));
+          const float f[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w)};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[4 * q + i] = jj == 0 ? f[i] : __fadd_rn(acc[4 * q + i], f[i]);
+        }
+      }
+      __nv_bfloat16 *out = p.d + (t.out_i0 + row) * p.ldd + t.out_j0 + 32 * c;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[i] = pack_bf16x2(__fmul_rn(alpha, acc[16 * h + 2 * i]), __fmul_rn(alpha, acc[16 * h + 2 * i + 1]));
+        st_global_v8(out + 16 * h, v);
+      }
+    }
+    named_barrier_sync(2, 128);  // the next pass overwrites the buffer
+  }
+}
+
 template <class C, bool GROUPED>
 __global__ void __launch_bounds__(320, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -208,6 +373,8 @@ __global__ void __launch_bounds__(320, 1)
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
+  volatile int *issued_count = consumed + 1;  // K stages the producer issued (abort drain)
+  volatile int *sk_last = consumed + 2;       // stream-K: epilogue decision broadcast
   int *tables = reinterpret_cast<int *>(ctrl + C::CTRL_BYTES);
   Tables<C, GROUPED> tb{tables, tables + (C::MAX_EXPERTS + 1), tables + 2 * (C::MAX_EXPERTS + 1)};
 
@@ -233,22 +400,10 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     *consumed = 0;
+    *issued_count = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-  }
-  int total_tiles = 0;
-  int tile0 = 0, tile_step = 1, split = 0;
-  if constexpr (!GROUPED) {
-    total_tiles = p.m_tiles * p.n_tiles;
-    if (p.splits > 1) {
-      tile0 = blockIdx.x / p.splits;
-      split = blockIdx.x % p.splits;
-      tile_step = total_tiles;  // exactly one tile per CTA
-    } else {
-      tile0 = blockIdx.x;
-      tile_step = gridDim.x;
-    }
   }
   if constexpr (GROUPED) {
     // Row offsets are produced by earlier kernels: read them only after the PDL wait.
@@ -280,11 +435,7 @@ __global__ void __launch_bounds__(320, 1)
   }
 
   __syncthreads();  // barriers initialised (and expert tables written, grouped)
-  if constexpr (GROUPED) {
-    total_tiles = tb.tp[p.experts];
-    tile0 = blockIdx.x;
-    tile_step = gridDim.x;
-  }
+  const Work work0 = make_work<GROUPED>(p, GROUPED ? tb.tp[p.experts] : 0);
   // The loader (warp 0) starts right away; warp 1 allocates tensor memory meanwhile and a named
   // barrier among warps 1..9 (the tensor-memory users) publishes its address.
   uint32_t tmem = 0;
@@ -312,11 +463,13 @@ __global__ void __launch_bounds__(320, 1)
     // activation half follows in the loop below.
     int pre = 0;
     const bool pre_a = p.weight_operand == 1, pre_b = p.weight_operand == 2;
-    if (!GROUPED && (pre_a || pre_b) && tile0 < total_tiles) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile0, split);
-      pre = min(C::STAGES, t.kt1 - t.kt0);
+    Work w = work0;
+    Seg s0;
+    if (!GROUPED && (pre_a || pre_b) && Work(work0).next(p, s0)) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
+      pre = min(C::STAGES, s0.kt1 - s0.kt0);
       for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
-        const int kt = t.kt0 + i;
+        const int kt = s0.kt0 + i;
         if (lane == 0) {
           const int nch = stage_chunks<C>(p, kt);
           mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
@@ -326,14 +479,15 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     pdl_wait();
-    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
-      for (int kt = t.kt0; kt < t.kt1; ++kt) {
-        const bool early_stage = tile == tile0 && kt - t.kt0 < pre;
+    bool first = true;
+    for (Seg sg; w.next(p, sg); first = false) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+      for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
+        const bool early_stage = first && kt - sg.kt0 < pre;
         if (!early_stage) {
           int ok = 1;
           if (lane == 0) {
-            ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc) ? 1 : 0;
+            ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty) ? 1 : 0;
             if (ok) {
               const int nch = stage_chunks<C>(p, kt);
               mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
@@ -354,50 +508,65 @@ __global__ void __launch_bounds__(320, 1)
   producer_done:
     if (lane == 0) {
       // remember how many stages were issued for the abort drain
-      reinterpret_cast<volatile int *>(tmem_holder)[3] = issued;
+      *issued_count = issued;
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // One wait per stage: the scale writers arrive on sff only after they saw the stage land
+    // (full), so sff covers both.  A full stage's four MMAs are issued unrolled with the
+    // accumulate predicates fixed (a runtime loop costs about a third more issue time).
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0;
+      int taken = 0;  // stages known landed (abort drain)
       int acc = 0;
       uint32_t acc_phase = 0;
       uint32_t it = 0;
-      for (int tile = tile0; tile < total_tiles; tile += tile_step) {
-        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
-        if (t.kt1 <= t.kt0) continue;  // no K work (never planned: splits <= K stages)
-        if (!mbar_wait(smem_u32(&acce[acc]), acc_phase ^ 1, wc)) goto mma_done;
+      Work w = work0;
+      for (Seg sg; w.next(p, sg);) {
+        if (!mbar_wait(smem_u32(&acce[acc]), acc_phase ^ 1, wc, kSiteMmaAcc)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * C::BN;
-        for (int kt = t.kt0; kt < t.kt1; ++kt, ++it) {
+        for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
           const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-          if (!mbar_wait(smem_u32(&full[stage]), phase, wc)) goto mma_done;
-          *consumed = *consumed + 1;
-          if (!mbar_wait(smem_u32(&sff[s_idx]), s_round & 1, wc)) goto mma_done;
+          if (!mbar_wait(smem_u32(&sff[s_idx]), s_round & 1, wc, kSiteMmaScale)) goto mma_done;
+          ++taken;
           tc_fence_after();
           const uint8_t *st = smem + stage * C::STAGE_BYTES;
           const uint32_t slot = tmem + C::SF_COL0 + s_idx * C::SF_SLOT;
-          const int nmma = stage_mmas(p, kt);
           const uint64_t adesc = sdesc_k_sw128(smem_u32(st)), bdesc = sdesc_k_sw128(smem_u32(st + C::A_BYTES));
-          for (int j = 0; j < nmma; ++j) {
-            const uint32_t accumulate = (kt > t.kt0 || j > 0) ? 1u : 0u;
-            if constexpr (C::MX) {
-              const int c = j >> 1;
-              const uint32_t id = (j & 1) * 2;
-              mma_mxf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC | (id << 29) | (id << 4),
-                       slot + 4 * c, slot + C::SFA_COLS + c * 4 * C::SFB_BLOCKS, accumulate);
+          const uint32_t acc0 = kt > sg.kt0 ? 1u : 0u;
+          if constexpr (C::MX) {
+            // MXFP4: a 512-byte scale chunk covers 128 K elements = two MMAs (scale ids 0, 2)
+            constexpr uint32_t I0 = C::IDESC, I2 = C::IDESC | (2u << 29) | (2u << 4);
+            const uint32_t sb = slot + C::SFA_COLS;
+            if (stage_mmas(p, kt) == 4) {
+              mma_mxf4(d_tmem, adesc, bdesc, I0, slot, sb, acc0);
+              mma_mxf4(d_tmem, adesc + 2, bdesc + 2, I2, slot, sb, 1u);
+              mma_mxf4(d_tmem, adesc + 4, bdesc + 4, I0, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
+              mma_mxf4(d_tmem, adesc + 6, bdesc + 6, I2, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
             } else {
-              mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j,
-                       slot + C::SFA_COLS + j * 4 * C::SFB_BLOCKS, accumulate);
+              for (int j = 0; j < stage_mmas(p, kt); ++j) {
+                const int c = j >> 1;
+                mma_mxf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, (j & 1) ? I2 : I0, slot + 4 * c,
+                         sb + c * 4 * C::SFB_BLOCKS, j > 0 ? 1u : acc0);
+              }
+            }
+          } else {
+            const uint32_t sb = slot + C::SFA_COLS;
+            constexpr uint32_t SB = 4 * C::SFB_BLOCKS;  // B scale columns per MMA
+            if (stage_mmas(p, kt) == 4) {
+              mma_nvf4(d_tmem, adesc, bdesc, C::IDESC, slot, sb, acc0);
+              mma_nvf4(d_tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
+              mma_nvf4(d_tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
+              mma_nvf4(d_tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
+            } else {
+              for (int j = 0; j < stage_mmas(p, kt); ++j)
+                mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB, j > 0 ? 1u : acc0);
             }
           }
           tc_commit(smem_u32(&empty[stage]));
           tc_commit(smem_u32(&sfe[s_idx]));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (++stage == C::STAGES) stage = 0;
         }
         tc_commit(smem_u32(&accf[acc]));
         if (++acc == C::NACC) {
@@ -405,7 +574,8 @@ __global__ void __launch_bounds__(320, 1)
           acc_phase ^= 1;
         }
       }
-    mma_done:;
+    mma_done:
+      *consumed = taken;
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ scale writers
@@ -416,13 +586,12 @@ __global__ void __launch_bounds__(320, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t it = 0;
-    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
-      if (t.kt1 <= t.kt0) continue;
-      for (int kt = t.kt0; kt < t.kt1; ++kt, ++it) {
+    Work w = work0;
+    for (Seg sg; w.next(p, sg);) {
+      for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
         const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-        if (!mbar_wait(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc)) goto scale_done;
-        if (!mbar_wait(smem_u32(&full[stage]), phase, wc)) goto scale_done;
+        if (!mbar_wait(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc, kSiteScaleSlot)) goto scale_done;
+        if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
         const uint32_t sfa_s = smem_u32(smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
         const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
         uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
@@ -462,24 +631,40 @@ __global__ void __launch_bounds__(320, 1)
     pdl_wait();
     const int quad = warp & 3;  // tcgen05.ld: warp w reaches lanes 32*(w%4) .. +31
     const int row = quad * 32 + lane;
+    const int tid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
     const float alpha = p.alpha ? *p.alpha : 1.0f;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, tile, split);
-      if (t.kt1 <= t.kt0) continue;  // no K work (never planned), mirrors the MMA issuer
-      if (!mbar_wait(smem_u32(&accf[acc]), acc_phase, wc)) break;
+    Work w = work0;
+    Seg pending{};  // a split tile this CTA must finish once its ring is idle
+    bool has_pending = false;
+    // After a failed wait the warps keep walking the segments without doing work (every later
+    // wait returns at once), so all four always meet the same named barriers.
+    for (Seg sg; w.next(p, sg);) {
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+      const bool sk_part = !GROUPED && p.splits == 1 && sg.n > 1;
+      const bool ok = mbar_wait(smem_u32(&accf[acc]), acc_phase, wc, kSiteEpilogue);
       tc_fence_after();
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
       float *red = reinterpret_cast<float *>(smem);
+      float *slot = sk_part ? sk_slot<C>(p, blockIdx.x, sg.j) : nullptr;
 #pragma unroll 1
-      for (int c = 0; c < C::BN / 32; ++c) {
+      for (int c = 0; ok && c < C::BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_base + 32 * c, r);
         tmem_ld_wait();
         if (p.splits > 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
+        } else if (sk_part) {
+          float *dst = slot + (c * 128 + row) * 32;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = r[8 * q + i];
+            st_global_v8(dst + 8 * q, v);
+          }
         } else if (!p.swap) {
           if (row < t.rows && 32 * c < t.cols) {
             __nv_bfloat16 *out = p.d + (t.out_i0 + row) * p.ldd + t.out_j0 + 32 * c;
@@ -512,6 +697,41 @@ __global__ void __launch_bounds__(320, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+      if (sk_part) {
+        // Publish the partial: the four warps' stores are ordered before one acquire-release
+        // increment of the tile's counter; the CTA that brings it to n adds the partials and
+        // sets it back to zero for the next call.
+        named_barrier_sync(2, 128);
+        if (tid == 0) {
+          int last = -1;  // -1: a wait gave up, do nothing more
+          if (!*abort_flag) {
+            unsigned int *cnt = p.ws_cnt + (sg.tile - p.dp_tiles);
+            last = atom_add_acq_rel_gpu(cnt, 1u) == static_cast<unsigned int>(sg.n - 1) ? 1 : 0;
+            if (last) *reinterpret_cast<volatile unsigned int *>(cnt) = 0u;
+          }
+          *sk_last = last;
+        }
+        named_barrier_sync(2, 128);
+        if (*sk_last == 1) {
+          // The ring is idle once no segment follows (all stages consumed, none to load); a
+          // split tile finished earlier waits for that point (at most one: only a CTA's first
+          // segment can be a partial that is not its last).
+          Work rest = w;
+          Seg more;
+          if (!rest.next(p, more)) {
+            sk_fixup<C>(p, t, sg, alpha, tid, smem);
+          } else {
+            pending = sg;
+            has_pending = true;
+          }
+        }
+      }
+    }
+    if (has_pending) {  // uniform over the four warps
+      named_barrier_sync(2, 128);
+      if (tid == 0) *sk_last = *abort_flag ? -1 : 1;  // after a time-out copies may still land in the ring
+      named_barrier_sync(2, 128);
+      if (*sk_last == 1) sk_fixup<C>(p, tile_info<C, GROUPED>(p, tb, pending.tile), pending, alpha, tid, smem);
     }
   }
 
@@ -521,7 +741,7 @@ __global__ void __launch_bounds__(320, 1)
     // Drain: wait (bounded) for copies still landing in shared memory and for outstanding
     // tcgen05 operations, so nothing writes shared or tensor memory after the CTA is gone.
     if (threadIdx.x == 0) {
-      const int issued = reinterpret_cast<volatile int *>(tmem_holder)[3];
+      const int issued = *issued_count;
       const int done = *consumed;
       for (int i = (done > issued - C::STAGES ? done : issued - C::STAGES); i < issued; ++i) {
         const uint32_t bar = smem_u32(&full[i % C::STAGES]);
@@ -549,7 +769,10 @@ __global__ void __launch_bounds__(320, 1)
       if (warp >= 2 && warp < 6) {
         const int tid = threadIdx.x - 64;  // 0..127
         const int rank = static_cast<int>(cluster_ctarank());
-        const TileInfo t = tile_info<C, GROUPED>(p, tb, tile0, split);
+        Work w = work0;
+        Seg sg{};
+        w.next(p, sg);
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
         const float alpha = p.alpha ? *p.alpha : 1.0f;
         constexpr int UNITS = C::BN * 128 / 4;  // float4 groups in the tile
         const int u0 = rank * UNITS / p.splits, u1 = (rank + 1) * UNITS / p.splits;

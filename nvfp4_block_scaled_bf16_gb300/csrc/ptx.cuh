@@ -45,7 +45,8 @@ struct WaitCtl {
   volatile int *abort;     // shared-memory flag: some role of this CTA gave up
   unsigned int *status;    // device status word read by nvfp4_check_status
 };
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w) {
+// Bounded wait; on expiry sets bit 0 of the status word and bit 8 + site (which wait gave up).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
@@ -53,7 +54,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     if (*w.abort) return false;
     if (clock64() - t0 > w.limit) {
       *w.abort = 1;
-      atomicOr(w.status, 1u);
+      atomicOr(w.status, 1u | (1u << (8 + site)));
       return false;
     }
   }
@@ -98,6 +99,20 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
 }
 
 // ---------------------------------------------------------------- PDL
+// 16-byte global -> shared copy that bypasses L1 (cp.async, completion by cp.async.wait_all).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Acquire-release atomic add at GPU scope; returns the old value.
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int *p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -28,7 +28,8 @@ def _declared():
 def test_header_declares_the_boundary():
     names = _declared()
     for want in ("nvfp4_quantize", "nvfp4_gemm", "mxfp4_quantize", "mxfp4_grouped_gemm", "sf_swizzle",
-                 "nvfp4_last_error", "nvfp4_sf_bytes", "nvfp4_check_status", "nvfp4_gemm_plan"):
+                 "nvfp4_last_error", "nvfp4_sf_bytes", "nvfp4_check_status", "nvfp4_gemm_plan",
+                 "nvfp4_gemm_workspace_size"):
         assert want in names
 
 
@@ -52,16 +53,41 @@ def test_size_queries(lib):
 
 
 def test_plan_selector_buckets(lib):
+    """Without a device the selector plans for 152 SMs."""
     for m in (1, 4, 8, 16):
         p = lib.nvfp4_gemm_plan(m, 4096, 7168)
-        assert p["swap_ab"] == 1 and p["tile_n"] == 32 and 1 <= p["splits"] <= 8
+        # 32 weight tiles, K split 4 ways inside clusters: 128 CTAs
+        assert p["swap_ab"] == 1 and p["tile_n"] == 32 and p["splits"] == 4
+        assert p["dp_tiles"] == 32 and p["sk_tiles"] == 0 and p["ctas"] == 128
     assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
     big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
-    assert big["swap_ab"] == 0 and big["splits"] == 1 and big["ctas"] <= 152
+    # 512 tiles of 128x256, walked whole and persistently
+    assert big["swap_ab"] == 0 and big["tile_n"] == 256 and big["ctas"] == 152
+    assert big["dp_tiles"] == 512 and big["sk_tiles"] == 0
+    small = lib.nvfp4_gemm_plan(32, 1024, 1024)            # 8 tiles x 4 stages: one stage per CTA
+    assert small["splits"] == 4 and small["ctas"] == 32
+    few = lib.nvfp4_gemm_plan(640, 1024, 2048)             # 40 tiles but only 2 stages per SM
+    assert few["sk_tiles"] == 0 and few["ctas"] == 40
+    deep = lib.nvfp4_gemm_plan(300, 1024, 16384)           # 24 tiles x 64 stages: stream-K
+    assert deep["sk_tiles"] == 24 and deep["dp_tiles"] == 0 and deep["ctas"] == 152
     for m in (1, 32, 256, 1024, 4096):
         p = lib.nvfp4_gemm_plan(m, 4096, 7168)
         assert p["ctas"] >= 1 and p["stages"] >= 2
+        if p["swap_ab"]:   # weight rows in 128-row tiles x token columns in tile_n tiles
+            tiles = 32 * -(-m // p["tile_n"])
+        else:
+            tiles = -(-m // 128) * (4096 // p["tile_n"])
+        assert p["dp_tiles"] + p["sk_tiles"] == tiles
+
+
+def test_workspace_size(lib):
+    """Counters (one per split tile, padded to 256 B) + 2 fp32 slots of 128 x tile_n per CTA."""
+    assert lib.gemm_workspace_size(1, 4096, 7168) == 0        # cluster split-K needs none
+    assert lib.gemm_workspace_size(4096, 4096, 7168) == 0     # whole tiles
+    assert lib.gemm_workspace_size(300, 1024, 16384) == 256 + 152 * 2 * 128 * 128 * 4
+    assert lib.gemm_workspace_size(2048, 512, 65536) == 256 + 152 * 2 * 128 * 128 * 4
+    assert lib.gemm_workspace_size(0, 4096, 7168) == 0
 
 
 def _c(v):
@@ -71,16 +97,16 @@ def _c(v):
 def test_gemm_rejects_bad_arguments_without_a_device(lib):
     L = lib.lib
     A, S, D = 0x10000, 0x20000, 0x30000  # never dereferenced: validation fails first
-    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1000, 0, None) == 3  # k % 32
-    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1000, 1024, 0, None) == 3  # n % 32
-    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), -1, 1024, 1024, 0, None) == 1
-    assert L.nvfp4_gemm(None, _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 1
-    assert L.nvfp4_gemm(_c(A + 16), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 2
-    assert L.nvfp4_gemm(_c(A), _c(S + 8), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 0, None) == 2
-    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, 1 << 20, None) == 1
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1000, None, 0, 0, None) == 3  # k % 32
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1000, 1024, None, 0, 0, None) == 3  # n % 32
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), -1, 1024, 1024, None, 0, 0, None) == 1
+    assert L.nvfp4_gemm(None, _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, None, 0, 0, None) == 1
+    assert L.nvfp4_gemm(_c(A + 16), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, None, 0, 0, None) == 2
+    assert L.nvfp4_gemm(_c(A), _c(S + 8), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, None, 0, 0, None) == 2
+    assert L.nvfp4_gemm(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 32, 1024, 1024, None, 0, 1 << 20, None) == 1
     assert "k" in lib.last_error() or "flags" in lib.last_error()
     # zero rows: a legal no-op that needs no device
-    assert L.nvfp4_gemm(None, None, None, None, None, None, 0, 1024, 1024, 0, None) == 0
+    assert L.nvfp4_gemm(None, None, None, None, None, None, 0, 1024, 1024, None, 0, 0, None) == 0
 
 
 def test_quantizers_reject_bad_arguments_without_a_device(lib):

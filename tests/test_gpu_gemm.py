@@ -49,6 +49,53 @@ def test_shapes_and_ragged_tails(nv, m, n, k):
     assert_within(d, R, tol, f"{m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (300, 1024, 16384),   # 24 tiles x 64 K stages over 152 CTAs: up to 8 contributors per tile
+    (1100, 256, 16384),   # BN=128, 18 tiles x 64 stages: tails of 76 rows in the last row block
+    (512, 512, 16384),    # 16 tiles x 64 stages
+    (2048, 512, 8224)])   # 64 tiles of 128x128, K tail of 32 (a short last stage)
+def test_stream_k_splits(nv, m, n, k):
+    """Shapes whose plan splits tiles stream-K (few tiles, long K), including ragged rows and a
+    K tail; every output element checked."""
+    p = nv.nvfp4_gemm_plan(m, n, k)
+    assert p["sk_tiles"] > 0
+    ops = nvfp4_operands(m, n, k, seed=11)
+    d = _run(nv, ops)
+    R, tol = reference(ops)
+    assert_within(d, R, tol, f"stream-K {m}x{n}x{k}")
+
+
+def test_workspace_contract(nv):
+    """An explicit workspace works, comes back all zero, gives bit-identical output on reuse;
+    a short or missing workspace is refused before anything is launched."""
+    m, n, k = 512, 512, 16384
+    ops = nvfp4_operands(m, n, k, 0)
+    args = (dev(ops["qa"]), dev(ops["sfa"]), dev(ops["qb"]), dev(ops["sfb"]), scalar(ops["alpha"]))
+    need = nv.gemm_workspace_size(m, n, k)
+    assert need > 0
+    ws = nv.gemm_workspace(need)
+    d0 = nv.nvfp4_gemm(*args, workspace=ws)
+    d1 = nv.nvfp4_gemm(*args, workspace=ws)
+    torch.cuda.synchronize()
+    nv.check_status()
+    assert int(torch.count_nonzero(ws[:256])) == 0          # arrival counters reset
+    assert torch.equal(d0, d1)
+    R, tol = reference(ops)
+    assert_within(d0, R, tol, "explicit workspace")
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_gemm(*args, workspace=ws[: need - 1])
+    assert e.value.code == 1 and "workspace" in str(e.value)
+    with pytest.raises(nv.NVFP4Error) as e:
+        nv.nvfp4_gemm(*args, workspace=ws[1:])
+    assert e.value.code in (1, 2)
+    L = nv.lib
+    import ctypes
+    c = lambda t: ctypes.c_void_p(t.data_ptr())
+    d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    assert L.nvfp4_gemm(c(args[0]), c(args[1]), c(args[2]), c(args[3]), c(args[4]), c(d), m, n, k, None, 0, 0,
+                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 1
+
+
 @pytest.mark.parametrize("m", [1, 4, 8, 16, 32, 64, 128, 256])
 def test_decode_sweep_full_size(nv, m):
     """N=4096, K=7168 with 0.1% outlier channels, every output element checked."""

@@ -18,12 +18,14 @@ def nv():
     return m
 
 
-@pytest.mark.parametrize("m,n,k", [(8, 1024, 2048), (512, 512, 1024)])
+@pytest.mark.parametrize("m,n,k", [(8, 1024, 2048), (512, 512, 1024), (512, 512, 16384)])
 def test_wait_times_out_and_context_survives(nv, m, n, k):
     ops = nvfp4_operands(m, n, k, 4)
     args = (dev(ops["qa"]), dev(ops["sfa"]), dev(ops["qb"]), dev(ops["sfb"]), scalar(ops["alpha"]))
     nv.check_status()                                    # start from a clean status word
-    nv.nvfp4_gemm(*args, flags=nv.FLAG_DEBUG_TIMEOUT | nv.FLAG_DEBUG_SKIP_FIRST_LOAD)
+    # a timed-out call may leave split-tile counters set: it gets a workspace of its own
+    ws = nv.gemm_workspace(nv.gemm_workspace_size(m, n, k))
+    nv.nvfp4_gemm(*args, flags=nv.FLAG_DEBUG_TIMEOUT | nv.FLAG_DEBUG_SKIP_FIRST_LOAD, workspace=ws)
     with pytest.raises(nv.NVFP4Error) as e:
         nv.check_status()
     assert e.value.code == 6                             # NVFP4_ERR_TIMEOUT
