@@ -171,6 +171,26 @@ nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b
                           void *workspace, size_t workspace_bytes, uint32_t flags,
                           nvfp4_stream_t stream);
 
+/* nvfp4_gemm without a workspace argument: when the plan splits tiles stream-K, the partial
+ * tiles and arrival counters go to a static 20 MiB device array inside the library instead of a
+ * caller buffer.  The pages have no counterpart of this entry point: it exists for callers that
+ * cannot allocate or hold device memory for a workspace at call time, such as a plugin inside an
+ * inference engine whose device memory is planned once up front, or code on a latency path where
+ * a cudaMalloc would synchronise the device.
+ *   Arguments, layouts, alignment and errors are those of nvfp4_gemm.  The call never allocates.
+ *   Shapes whose workspace (nvfp4_gemm_workspace_size) exceeds 20 MiB are refused with
+ *   NVFP4_ERR_UNSUPPORTED_SHAPE; every plan the selector makes on a GPU of up to 160 SMs fits.
+ *   The array is shared by every call on the device: calls that may overlap (other streams,
+ *   other threads) race on it and must not use this entry point concurrently.
+ *   The array's address is looked up on the first call on each device (cudaGetSymbolAddress);
+ *   a caller that records work for later replay should make one call before it starts recording.
+ *   The arrival counters must read zero when the kernel starts: before each launch of a split
+ *   plan this entry point clears them with cudaMemsetAsync on `stream` (so a call after one
+ *   that timed out starts clean); the partial-tile slots need no initialisation. */
+nvfp4_status_t nvfp4_gemm_noalloc(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb,
+                                  const float *alpha, void *d, int64_t m, int64_t n, int64_t k,
+                                  uint32_t flags, nvfp4_stream_t stream);
+
 /* MXFP4 grouped (MoE) GEMM: for every expert e, D[rows of e, :] = alpha * deq(A_e) deq(B_e)^T.
  * The kernel checks row_offsets on the device (row_offsets[0] == 0, row_offsets[E] == t,
  * non-decreasing); if they are malformed it does no work and nvfp4_check_status reports

@@ -43,6 +43,7 @@ _SIGS = {
     "nvfp4_gemm_plan": (_int, [_i64, _i64, _i64, ctypes.POINTER(PlanT)]),
     "nvfp4_gemm_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
     "nvfp4_gemm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
+    "nvfp4_gemm_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_check_status": (_int, [_vp]),
@@ -197,6 +198,30 @@ def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None, works
     _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
                            _ptr(workspace), 0 if workspace is None else workspace.numel(), flags,
                            _stream(stream)))
+    return d
+
+
+def nvfp4_gemm_noalloc(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None):
+    """nvfp4_gemm with the library's static split-K scratch instead of a workspace (never
+    allocates on the device beyond the output when d is None).  Not for concurrent use."""
+    _need(a, torch.uint8, "a", 2)
+    _need(b, torch.uint8, "b", 2)
+    _need(sfa, torch.uint8, "sfa")
+    _need(sfb, torch.uint8, "sfb")
+    _need(alpha, torch.float32, "alpha")
+    m, kh = a.shape
+    n = b.shape[0]
+    if b.shape[1] != kh:
+        raise ValueError("a and b disagree on K")
+    for t_, name in ((a, "a"), (b, "b")):
+        if not t_.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if sfa.numel() < sf_bytes(m, 2 * kh) or sfb.numel() < sf_bytes(n, 2 * kh):
+        raise ValueError("scale buffers are too small")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _check(_lib.nvfp4_gemm_noalloc(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
+                                   flags, _stream(stream)))
     return d
 
 
