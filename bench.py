@@ -16,10 +16,12 @@ Workloads (synthetic, seeded; shapes and value distributions of the pages' bench
   moe                 MXFP4: 4096 tokens top-8 over 128 experts (32768 rows); quantise, then the
                       gate+up grouped GEMM (N=1536, K=2048) and the down grouped GEMM (N=2048,
                       K=768) on a second quantised activation.
-Each step is captured once in a CUDA graph and replayed; the L2 is flushed (a 512 MB write)
-before every timed step, outside the timed interval.  `value` is GEMM TFLOPS over the whole
-step (quantisation time included); `roofline` covers the GEMM kernel, timed on its own in a
-second graph of the step's GEMM launches.
+Each step is captured once in a CUDA graph and replayed; the L2 is flushed before every timed
+step, outside the timed interval: a 512 MB write, then a 512 MB read of a second buffer, so the
+step starts with none of its inputs in L2 and with L2 holding clean lines (as after the previous
+layer's kernels), not 126 MB of dirty lines whose write-back would compete with the step's
+reads.  `value` is GEMM TFLOPS over the whole step (quantisation time included); `roofline`
+covers the GEMM kernel, timed on its own in a second graph of the step's GEMM launches.
 """
 from __future__ import annotations
 
@@ -204,7 +206,7 @@ def make_decode(nv):
     wl.config = {"workload": "decode sweep: NVFP4 quant->GEMM, N=4096 K=7168, M in 1,4,8,16,32,64,128,256",
                  "global_batch": sum(DECODE_MS), "n": 4096, "k": 7168, "ms": list(DECODE_MS),
                  "inputs": "activation N(0,1) with 0.1% outlier channels x20, weight N(0,0.02), seed 0",
-                 "l2": "flushed (512 MB write) before every timed step; 8 distinct weight copies",
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read); 8 distinct weight copies",
                  "parallelism": "replicas"}
     return wl
 
@@ -215,7 +217,7 @@ def make_prefill(nv):
     wl.config = {"workload": "prefill sweep: NVFP4 quant->GEMM, (M,N,K) in " + str(list(PREFILL)),
                  "global_batch": sum(s[0] for s in PREFILL),
                  "inputs": "activation N(0,1) with 0.1% outlier channels x20, weight N(0,0.02), seed 0",
-                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
     return wl
 
 
@@ -225,7 +227,7 @@ def make_e2e(nv, pdl=True):
     wl.config = {"workload": "quant->GEMM with PDL: act bf16 [M,4096], M in 256,512, weight [14336,4096]",
                  "global_batch": 768, "pdl": pdl,
                  "inputs": "activation N(0,1) with outlier channels x20, weight N(0,0.02), seed 0",
-                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
     return wl
 
 
@@ -263,7 +265,7 @@ def make_moe(nv):
                              "down N=2048 K=768; quant + grouped GEMM each",
                  "global_batch": rows, "expert_rows_min": int(counts.min()), "expert_rows_max": int(counts.max()),
                  "inputs": "activation N(0,1), weight N(0,0.02), router logits N(0,1), seed 0",
-                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
     return wl
 
 
@@ -271,7 +273,7 @@ def make_custom(nv, shapes):
     wl = Workload(nv, "custom")
     build_nvfp4_chain(nv, wl, shapes)
     wl.config = {"workload": "NVFP4 quant->GEMM chain " + str(shapes), "global_batch": sum(s[0] for s in shapes),
-                 "l2": "flushed (512 MB write) before every timed step", "parallelism": "replicas"}
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
     return wl
 
 
@@ -295,12 +297,25 @@ def capture(fns) -> torch.cuda.CUDAGraph:
     return g
 
 
-def timed_replays(g, n: int, flush: torch.Tensor, before=None, after=None) -> list[float]:
+class L2Flush:
+    """Evicts the step's data from L2: writes a 512 MB buffer, then reads a second one, so what
+    L2 holds afterwards is clean (no write-backs land inside the timed interval)."""
+
+    def __init__(self):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(128 << 20, dtype=torch.int32, device="cuda")
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xFF)
+        self.r.sum()
+
+
+def timed_replays(g, n: int, flush: L2Flush, before=None, after=None) -> list[float]:
     """Per-replay device times (ms), each after an L2 flush outside the timed interval."""
     out = []
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
-        flush.fill_(i & 0xFF)
+        flush(i)
         a, b = evs[i]
         a.record()
         if before:
@@ -339,7 +354,7 @@ def run_ours(args, dist_on, rank, world):
         wl = make_custom(nv, shapes)
     else:
         wl = MAKERS[args.workload](nv)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     step_graph = capture(wl.launches)
     gemm_graph = capture(wl.gemm_launches)
     for _ in range(args.warmup):
@@ -357,9 +372,12 @@ def run_ours(args, dist_on, rank, world):
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dist_on)
 
     # ---- GEMM kernels alone (roofline of the dominant kernel)
-    gemm_ms = timed_replays(gemm_graph, max(3, min(args.steps, 50)), flush)
-    per_launch_ms = statistics.median(gemm_ms) / len(wl.gemm_launches)
-    quant_ms = max(0.0, ms - statistics.median(gemm_ms))
+    # Means, not medians: CUDA events resolve these short graphs only to ~2 us, so a median
+    # snaps to that grid; the mean over many replays does not.
+    gemm_ms = timed_replays(gemm_graph, max(3, min(args.steps, 100)), flush)
+    gemm_mean = statistics.mean(gemm_ms)
+    per_launch_ms = gemm_mean / len(wl.gemm_launches)
+    quant_ms = max(0.0, ms - gemm_mean)
 
     # ---- end to end through the public API with host buffers
     def h2d():
@@ -377,9 +395,9 @@ def run_ours(args, dist_on, rank, world):
 
     hbm, bf16, peak_kind = peaks()
     tflops = wl.flops * world / (ms * 1e-3) / 1e12
-    gemm_gbs = wl.gemm_bytes / (statistics.median(gemm_ms) * 1e-3) / 1e9
+    gemm_gbs = wl.gemm_bytes / (gemm_mean * 1e-3) / 1e9
     fp4_peak_tflops = bf16 * 6.0  # nominal dense FP4 : bf16 ratio 13.5 : 2.25
-    gemm_tflops = wl.flops / (statistics.median(gemm_ms) * 1e-3) / 1e12
+    gemm_tflops = wl.flops / (gemm_mean * 1e-3) / 1e12
     # binding roof of the step's GEMMs: max(flops / FP4 peak, bytes / HBM)
     t_roof = max(wl.flops / (fp4_peak_tflops * 1e12), wl.gemm_bytes / (hbm * 1e9))
     bound = "hbm" if wl.gemm_bytes / (hbm * 1e9) >= wl.flops / (fp4_peak_tflops * 1e12) else "tensor"
@@ -393,7 +411,7 @@ def run_ours(args, dist_on, rank, world):
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak_tflops, 4), "traffic": None}
     roof.update({"kernel": "bs_gemm_kernel" if wl.name != "moe" else "bs_gemm_kernel (grouped)",
                  "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if bound == 'hbm' else 'bf16_tflops x 6, the nominal fp4/bf16 ratio'})",
-                 "per_launch_ms": round(per_launch_ms, 5), "binding_roof_frac": round(t_roof / (statistics.median(gemm_ms) * 1e-3), 4),
+                 "per_launch_ms": round(per_launch_ms, 5), "binding_roof_frac": round(t_roof / (gemm_mean * 1e-3), 4),
                  "bytes_per_step": wl.gemm_bytes})
 
     line = {"metric": METRIC, "value": round(tflops, 2), "unit": "TFLOPS", "n_gpus": world,
@@ -405,7 +423,7 @@ def run_ours(args, dist_on, rank, world):
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes},
             "gpu_launches": len(wl.launches) * args.steps,
             "clocks": clk,
-            "breakdown": {"gemm_ms": round(statistics.median(gemm_ms), 5), "quant_ms_est": round(quant_ms, 5),
+            "breakdown": {"gemm_ms": round(gemm_mean, 5), "quant_ms_est": round(quant_ms, 5),
                           "quant_bytes_per_step": wl.quant_bytes, "wall_s": round(wall, 3)}}
     if wl.name == "decode":
         line["pages_b300_context"] = {

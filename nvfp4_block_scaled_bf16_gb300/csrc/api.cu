@@ -117,6 +117,31 @@ nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t in
   return NVFP4_OK;
 }
 
+nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_t k_bytes, uint64_t rows,
+                                     uint32_t box_rows, uint32_t box_stages) {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                    cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  if (k_bytes % 128 != 0) return fail(NVFP4_ERR_INVALID_ARG, "stage view needs K %% 256 == 0");
+  cuuint64_t dims[3] = {128, rows, k_bytes / 128};
+  cuuint64_t strides[2] = {k_bytes, 128};
+  cuuint32_t box[3] = {128, box_rows, box_stages};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled (stage view) failed (%d) for %llu x %llu bytes",
+                static_cast<int>(r), static_cast<unsigned long long>(rows), static_cast<unsigned long long>(k_bytes));
+  return NVFP4_OK;
+}
+
 nvfp4_status_t allow_smem(const void *fn, int bytes, int device) {
   {
     std::lock_guard<std::mutex> lock(g_mu);

@@ -10,7 +10,11 @@
 //             shared memory (decode shapes are weight-streaming, so every SM must pull).
 //             Measured against a stream-K split through the workspace, the cluster reduction
 //             was 2 us faster at M <= 32 and 2x faster at M = 256, where one CTA would have to
-//             read every 128 KB partial of a tile.
+//             read every 128 KB partial of a tile (and against partials pushed into the owning
+//             CTA with st.async: 2 us faster per GEMM from cold L2).  When a CTA's K slice fits
+//             its ring the operands land with few copies ("resident"), and at most 3 stages per
+//             CTA are in flight: with cold HBM, requesting every stage at once made all of them
+//             land together, leaving no load for the MMAs to overlap.
 //   M >  256  128 x 256 tiles (128 x 128 when N is not a multiple of 256 or there are fewer
 //             256-wide tiles than SMs), persistent over the SMs, double-buffered accumulators
 //             where tensor memory allows.  When the tiles fill less than half the SMs and K is
@@ -26,6 +30,7 @@ namespace {
 
 struct Plan {
   int swap, bn, splits, stages, ctas, m_tiles, n_tiles, k_tiles, dp_tiles, sk_tiles;
+  int resident, nst_max, lookahead;  // see GemmArgs
   size_t ws_bytes;
 };
 
@@ -94,6 +99,14 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     case 128: pl.stages = 6; break;
     default: pl.stages = 4; break;
   }
+  // A swap-AB CTA holds one tile; when its whole K slice fits the ring (and K is a whole number of
+  // 256-wide stages), the activation and both scale slices land with one copy each.
+  pl.nst_max = static_cast<int>(ceil_div(pl.k_tiles, pl.splits));
+  pl.resident = pl.swap && k % 256 == 0 && pl.nst_max <= pl.stages && pl.bn <= 128;
+  // Weight-streaming (swap-AB) CTAs keep only a few stages in flight: when every CTA requests
+  // its whole slice at once, cold HBM completes all of a CTA's stages at about the same time and
+  // the MMAs cannot overlap the loads; paced requests land in order.
+  pl.lookahead = pl.swap ? 3 : 0;
   return pl;
 }
 
@@ -184,11 +197,17 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   const uint8_t *opa = pl.swap ? b : a, *opb = pl.swap ? a : b;
   const uint8_t *sfopa = pl.swap ? sfb : sfa, *sfopb = pl.swap ? sfa : sfb;
   const int64_t rows_a = pl.swap ? n : m, rows_b = pl.swap ? m : n;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tb3;
   st = encode_tmap_2d_u8(&ta, opa, k / 2, rows_a, k / 2, 128, 128, true);
   if (st != NVFP4_OK) return st;
   st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.bn, true);
   if (st != NVFP4_OK) return st;
+  if (pl.resident) {
+    st = encode_tmap_stages_u8(&tb3, opb, k / 2, rows_b, pl.bn, pl.nst_max);
+    if (st != NVFP4_OK) return st;
+  } else {
+    tb3 = tb;  // unused
+  }
 
   GemmArgs args{};
   args.sfa = sfopa;
@@ -212,6 +231,9 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.debug_skip_first_load = (flags & NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD) && (flags & NVFP4_FLAG_DEBUG_TIMEOUT);
   args.dp_tiles = pl.dp_tiles;
   args.sk_tiles = pl.sk_tiles;
+  args.resident = pl.resident;
+  args.nst_max = pl.nst_max;
+  args.lookahead = pl.lookahead;
   if (pl.sk_tiles > 0) {
     args.ws_cnt = static_cast<unsigned int *>(workspace);
     args.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
@@ -222,7 +244,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   return with_config(pl, [&](auto cfg) {
     using C = decltype(cfg);
     const cudaError_t e = launch(bs_gemm_kernel<C, false>, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
-                                 (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, args);
+                                 (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, tb3, args);
     return check_launch(e, "nvfp4_gemm");
   });
 }

@@ -10,8 +10,12 @@
 // 32q+i, column j holds the 4 bytes at tile offset 16*i + 4*j, the same in every quadrant.
 //
 // CTA = 10 warps:
-//   warp 0      TMA producer: A/B tiles (128-byte swizzle) and scale chunks (bulk copies)
-//               into a STAGES-deep shared-memory ring, one mbarrier pair per stage;
+//   warp 0      TMA producer (one thread issues every copy): A/B tiles (128-byte swizzle) and
+//               scale chunks (bulk copies) into a STAGES-deep shared-memory ring, one mbarrier
+//               pair per stage.  A single-tile CTA whose K slice fits the ring ("resident")
+//               lands B and both scale slices with one copy each and A stage by stage, the
+//               first copies going out before the rest of the CTA is set up; weight-streaming
+//               CTAs keep at most `lookahead` stages in flight so cold HBM returns them in order;
 //   warp 1      allocates tensor memory; one lane issues 4 MMAs (K = 64 each) per 256-wide K
 //               stage, then commits the stage back to the producer and the scale slot back to
 //               the scale writers, and after the last K stage of a tile the accumulator to the
@@ -20,7 +24,8 @@
 //               conversion to bf16, 256-bit stores;
 //   warps 6..9  scale writers: each reads the stage's scale tiles from shared memory and
 //               writes them into its own quadrant of a tensor-memory scale slot with
-//               tcgen05.st (SF_SLOTS slots in a ring), keeping those writes off the tensor pipe
+//               tcgen05.st (SF_SLOTS slots in a ring; a resident CTA fills one slot per stage
+//               with a single hand-off to the MMA lane), keeping those writes off the tensor pipe
 //               (a tcgen05.cp of one 512-byte tile occupies the pipe about as long as 40 % of a
 //               128x256x64 MMA).
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
@@ -74,10 +79,12 @@ struct GemmCfg {
   static constexpr int SFB_COLS = SFB_BLOCKS * CHUNKS * 4;
   static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // columns of one scale slot
   // a second accumulator only helps CTAs that walk several tiles (epilogue of tile t overlaps
-  // the mainloop of t+1); single-tile CTAs keep tensor memory small enough for two per SM
+  // the mainloop of t+1)
   static constexpr int NACC = (MULTI_TILE_ && 2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
   static constexpr int SF_COL0 = NACC * BN;
-  static constexpr int SF_SLOTS = (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
+  // Tensor-memory scale slots: one per ring stage for single-tile (swap-AB) CTAs, so a CTA
+  // whose K slice fits the ring writes every stage's scales once, with no slot reuse.
+  static constexpr int SF_SLOTS = !MULTI_TILE_ ? STAGES : (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int RED_BYTES = BM * BN * 4;  // partial tile: cluster split-K buffer, stream-K slot
@@ -85,16 +92,24 @@ struct GemmCfg {
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
   static constexpr int CTRL_BYTES = 512;
   static constexpr int THREADS = 320;
+  // The ring keeps each operand in a region of its own (stage i of A at A_REGION + i * A_BYTES,
+  // and so on), so the stages of one operand are contiguous and a CTA whose whole K slice fits
+  // the ring can land an operand's slice with a single copy.
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int B_REGION = STAGES * A_BYTES;
+  static constexpr int SFA_REGION = B_REGION + STAGES * B_BYTES;
+  static constexpr int SFB_REGION = SFA_REGION + STAGES * SFA_BYTES;
   // dynamic shared memory: alignment slack, stage ring, barriers, expert tables (grouped only)
   static constexpr int smem_bytes(bool grouped) {
-    return 1024 + STAGES * STAGE_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
+    return 1024 + RING_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
   }
   static constexpr uint32_t IDESC = idesc_block_scaled(BM, BN, MX, 0);
-  static_assert(TMEM_USED <= 512, "tensor memory budget");
-  static_assert((2 * STAGES + 13) * 8 + 6 * 4 <= CTRL_BYTES, "barriers and flags fit the control block");
+  static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8, "tensor memory budget, scale-slot barriers");
+  static_assert((2 * STAGES + 22) * 8 + 7 * 4 <= CTRL_BYTES, "barriers and flags fit the control block");
+  static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
-  static_assert(STAGE_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
 };
 
 struct GemmArgs {
@@ -119,6 +134,12 @@ struct GemmArgs {
   int sk_tiles;               // tiles [dp_tiles, dp_tiles + sk_tiles) are split stream-K
   float *ws;                  // stream-K: 2 partial-tile slots (BM x BN fp32) per CTA
   unsigned int *ws_cnt;       // stream-K: one arrival counter per split tile, zero between calls
+  int resident;               // 1: each CTA's K slice (at most nst_max stages) fits the ring and
+                              // K % 256 == 0: operand B and both scale slices land with one copy
+                              // each, operand A stage by stage (single-tile, non-grouped CTAs)
+  int nst_max;                // resident: K stages of the longest slice = z extent of tmB3's box
+  int lookahead;              // > 0: at most this many K stages in flight per CTA (stage i + L is
+                              // issued once stage i has landed); 0: as many as the ring holds
 };
 
 struct TileInfo {
@@ -187,8 +208,8 @@ __device__ __forceinline__ Work make_work(const GemmArgs &p, int grouped_tiles) 
     w.tile_step = 1;
     w.split = blockIdx.x % p.splits;
     w.splits = p.splits;
-    w.kt_lo = static_cast<int>(static_cast<int64_t>(w.split) * p.k_tiles / p.splits);
-    w.kt_hi = static_cast<int>(static_cast<int64_t>(w.split + 1) * p.k_tiles / p.splits);
+    w.kt_lo = w.split * p.k_tiles / p.splits;  // splits <= 8, k_tiles < 2^23: no overflow
+    w.kt_hi = (w.split + 1) * p.k_tiles / p.splits;
   } else {
     w.tile_end = p.dp_tiles;
     if (p.sk_tiles > 0) {
@@ -257,24 +278,25 @@ __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
   return min(4, (p.k - kt * 256 + 63) / 64);
 }
 
-// Copies of K stage kt into ring slot stg, one per lane: lane 0 the A tile, lane 1 the B tile,
-// lane 2 A's scale chunks, lanes 3.. B's scale blocks (only the requested operand halves).
+// Copies of K stage kt into ring slot stg (only the requested operand halves), all issued by the
+// calling thread: a copy instruction costs the issuing thread ~100 cycles whatever its size,
+// and spreading them over divergent lanes of one warp was measured slower still.
 template <class C>
 __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t, int kt, int stg, uint8_t *smem,
                                             uint64_t *full, const CUtensorMap *tmA, const CUtensorMap *tmB,
-                                            int lane, bool do_a, bool do_b) {
+                                            bool do_a, bool do_b) {
   const int nch = stage_chunks<C>(p, kt);
-  uint8_t *st = smem + stg * C::STAGE_BYTES;
   const uint32_t bar = smem_u32(&full[stg]);
-  uint8_t *sfa_s = st + C::A_BYTES + C::B_BYTES;
-  if (do_a && lane == 0) tma_load_2d(smem_u32(st), tmA, bar, kt * 128, t.a_y);
-  if (do_b && lane == 1) tma_load_2d(smem_u32(st + C::A_BYTES), tmB, bar, kt * 128, t.b_y);
-  if (do_a && lane == 2)
-    bulk_load(smem_u32(sfa_s), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
-  if (do_b && lane >= 3 && lane < 3 + t.sfb_blocks) {
-    const int b = lane - 3;
-    bulk_load(smem_u32(sfa_s + C::SFA_BYTES + b * C::CHUNKS * 512),
-              t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+  if (do_a) {
+    tma_load_2d(smem_u32(smem + stg * C::A_BYTES), tmA, bar, kt * 128, t.a_y);
+    bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512,
+              nch * 512, bar);
+  }
+  if (do_b) {
+    tma_load_2d(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt * 128, t.b_y);
+    for (int b = 0; b < t.sfb_blocks; ++b)
+      bulk_load(smem_u32(smem + C::SFB_REGION + stg * C::SFB_BYTES + b * C::CHUNKS * 512),
+                t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
   }
 }
 
@@ -359,22 +381,23 @@ __device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, c
 template <class C, bool GROUPED>
 __global__ void __launch_bounds__(320, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs p) {
+                   const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *ctrl = smem + C::STAGES * C::STAGE_BYTES;
+  uint8_t *ctrl = smem + C::RING_BYTES;
   uint64_t *full = reinterpret_cast<uint64_t *>(ctrl);
   uint64_t *empty = full + C::STAGES;
   uint64_t *accf = empty + C::STAGES;
   uint64_t *acce = accf + 2;
   uint64_t *sff = acce + 2;           // scale slot written (4 scale-writer warps arrive)
-  uint64_t *sfe = sff + 4;            // scale slot free (MMA commit)
-  uint64_t *drain = sfe + 4;
+  uint64_t *sfe = sff + 8;            // scale slot free (MMA commit)
+  uint64_t *drain = sfe + 8;
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
   volatile int *issued_count = consumed + 1;  // K stages the producer issued (abort drain)
   volatile int *sk_last = consumed + 2;       // stream-K: epilogue decision broadcast
+  volatile float *alpha_s = reinterpret_cast<volatile float *>(sk_last + 1);  // alpha, read once
   int *tables = reinterpret_cast<int *>(ctrl + C::CTRL_BYTES);
   Tables<C, GROUPED> tb{tables, tables + (C::MAX_EXPERTS + 1), tables + 2 * (C::MAX_EXPERTS + 1)};
 
@@ -393,7 +416,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(smem_u32(&accf[a]), 1);
       mbar_init(smem_u32(&acce[a]), 4);
     }
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < C::SF_SLOTS; ++q) {
       mbar_init(smem_u32(&sff[q]), 4);
       mbar_init(smem_u32(&sfe[q]), 1);
     }
@@ -402,6 +425,33 @@ __global__ void __launch_bounds__(320, 1)
     *consumed = 0;
     *issued_count = 0;
     fence_barrier_init();
+    if constexpr (!GROUPED) {
+      if (p.resident) {
+        // The CTA's one segment fits the ring: every copy goes out now, before the rest of the
+        // CTA is set up.  Stage i of A has barrier full[i]; the slices of A's scales, of B and
+        // of B's scales complete on full[0].  B's half waits for griddepcontrol.wait under PDL
+        // (it is the activation) and is issued by the producer warp below.
+        // (the segment and tile of make_work / tile_info, in 32-bit arithmetic: one tile per CTA)
+        const int sp = p.splits, cta = static_cast<int>(blockIdx.x);
+        const int tile = cta / sp, split = cta % sp;
+        const int kt0 = split * p.k_tiles / sp, nst = (split + 1) * p.k_tiles / sp - kt0;
+        const int mb = tile % p.m_tiles, b_y = (tile / p.m_tiles) * C::BN;
+        const uint8_t *sfa_blk = p.sfa + (static_cast<int64_t>(mb) * p.sf_chunks + kt0 * C::CHUNKS) * 512;
+        const uint8_t *sfb_blk = p.sfb + (static_cast<int64_t>(b_y / 128) * p.sf_chunks + kt0 * C::CHUNKS) * 512;
+        mbar_arrive_expect_tx(smem_u32(&full[0]), C::A_BYTES + p.nst_max * C::B_BYTES + nst * (C::SFA_BYTES + C::SFB_BYTES));
+        for (int i = 1; i < nst; ++i) mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES);
+        bulk_load(smem_u32(smem + C::SFA_REGION), sfa_blk, nst * C::SFA_BYTES, smem_u32(&full[0]));
+        const int first = p.lookahead > 0 && p.lookahead < nst ? p.lookahead : nst;
+        for (int i = 0; i < first; ++i)
+          if (!(p.debug_skip_first_load && i == 0))
+            tma_load_2d(smem_u32(smem + i * C::A_BYTES), &tmA, smem_u32(&full[i]), (kt0 + i) * 128, mb * 128);
+        if (p.weight_operand != 1) {
+          tma_load_3d(smem_u32(smem + C::B_REGION), &tmB3, smem_u32(&full[0]), 0, b_y, kt0);
+          bulk_load(smem_u32(smem + C::SFB_REGION), sfb_blk, nst * C::SFB_BYTES, smem_u32(&full[0]));
+        }
+        *issued_count = first;
+      }
+    }
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
   }
@@ -452,70 +502,116 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // Lane 0 keeps the ring bookkeeping and posts each stage's byte count; lanes 0-4 then issue
-    // the stage's copies in parallel (issue_stage).
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;
-    const bool skip_first = p.debug_skip_first_load != 0;
-    // Under PDL (p.weight_operand != 0) the weight half of the first ring of stages goes out
-    // before griddepcontrol.wait, so it streams while the preceding kernel finishes; the
-    // activation half follows in the loop below.
-    int pre = 0;
-    const bool pre_a = p.weight_operand == 1, pre_b = p.weight_operand == 2;
-    Work w = work0;
-    Seg s0;
-    if (!GROUPED && (pre_a || pre_b) && Work(work0).next(p, s0)) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
-      pre = min(C::STAGES, s0.kt1 - s0.kt0);
-      for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
-        const int kt = s0.kt0 + i;
-        if (lane == 0) {
-          const int nch = stage_chunks<C>(p, kt);
-          mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+    // One thread keeps the ring bookkeeping and issues every copy.
+    if (lane == 0) {
+      int issued = 0;
+      if (!GROUPED && p.resident) {
+        // Everything but B's half (the activation, under PDL) went out during set-up.
+        Seg s0;
+        if (Work(work0).next(p, s0)) {
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
+          if (p.weight_operand == 1) {
+            pdl_wait();
+            tma_load_3d(smem_u32(smem + C::B_REGION), &tmB3, smem_u32(&full[0]), 0, t.b_y, s0.kt0);
+            bulk_load(smem_u32(smem + C::SFB_REGION), t.sfb_blk + static_cast<int64_t>(s0.kt0) * C::CHUNKS * 512,
+                      (s0.kt1 - s0.kt0) * C::SFB_BYTES, smem_u32(&full[0]));
+          }
+          // the rest of A, paced: stage i goes out once stage i - lookahead has landed
+          issued = *issued_count;
+          for (int i = issued; i < s0.kt1 - s0.kt0; ++i) {
+            if (!mbar_wait(smem_u32(&full[i - p.lookahead]), 0, wc, kSiteLoadEmpty)) goto producer_done;
+            tma_load_2d(smem_u32(smem + i * C::A_BYTES), &tmA, smem_u32(&full[i]), (s0.kt0 + i) * 128, t.a_y);
+            issued = i + 1;
+          }
         }
-        __syncwarp();
-        if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, lane, pre_a, pre_b);
-      }
-    }
-    pdl_wait();
-    bool first = true;
-    for (Seg sg; w.next(p, sg); first = false) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
-      for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
-        const bool early_stage = first && kt - sg.kt0 < pre;
-        if (!early_stage) {
-          int ok = 1;
-          if (lane == 0) {
-            ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty) ? 1 : 0;
-            if (ok) {
+      } else {
+        int stage = 0;
+        uint32_t phase = 0;
+        const bool skip_first = p.debug_skip_first_load != 0;
+        // Under PDL (p.weight_operand != 0) the weight half of the first ring of stages goes out
+        // before griddepcontrol.wait, so it streams while the preceding kernel finishes; the
+        // activation half follows in the loop below.
+        int pre = 0;
+        const bool pre_a = p.weight_operand == 1, pre_b = p.weight_operand == 2;
+        Work w = work0;
+        Seg s0;
+        if (!GROUPED && (pre_a || pre_b) && Work(work0).next(p, s0)) {
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
+          pre = min(p.lookahead > 0 ? p.lookahead : C::STAGES, min(C::STAGES, s0.kt1 - s0.kt0));
+          for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
+            const int kt = s0.kt0 + i;
+            const int nch = stage_chunks<C>(p, kt);
+            mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+            if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
+          }
+        }
+        pdl_wait();
+        bool first = true;
+        for (Seg sg; w.next(p, sg); first = false) {
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+          for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
+            const bool early_stage = first && kt - sg.kt0 < pre;
+            if (p.lookahead > 0 && issued >= p.lookahead) {  // pacing: stage issued - L has landed
+              const int j = issued - p.lookahead;
+              if (!mbar_wait(smem_u32(&full[j % C::STAGES]), (j / C::STAGES) & 1, wc, kSiteLoadEmpty)) goto producer_done;
+            }
+            if (!early_stage) {
+              if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) goto producer_done;
               const int nch = stage_chunks<C>(p, kt);
               mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
             }
+            const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
+            if (!(skip_first && issued == 0) && (do_a || do_b))
+              issue_stage<C>(p, t, kt, stage, smem, full, &tmA, &tmB, do_a, do_b);
+            ++issued;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
-          if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) goto producer_done;
-        }
-        const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
-        if (!(skip_first && issued == 0) && (do_a || do_b))
-          issue_stage<C>(p, t, kt, stage, smem, full, &tmA, &tmB, lane, do_a, do_b);
-        ++issued;
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
         }
       }
-    }
-  producer_done:
-    if (lane == 0) {
-      // remember how many stages were issued for the abort drain
-      *issued_count = issued;
+    producer_done:
+      *issued_count = issued;  // stages issued, for the abort drain
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One wait per stage: the scale writers arrive on sff only after they saw the stage land
     // (full), so sff covers both.  A full stage's four MMAs are issued unrolled with the
     // accumulate predicates fixed (a runtime loop costs about a third more issue time).
-    if (lane == 0) {
+    if (lane == 0 && !GROUPED && p.resident) {
+      // Resident slice: the scale writers fill every stage's scale slot once (one hand-off);
+      // the MMAs of stage i then only wait for A's stage i to land.
+      int taken = 0;
+      Seg sg;
+      Work w = work0;
+      if (w.next(p, sg)) {
+        const int nst = sg.kt1 - sg.kt0;
+        if (!mbar_wait(smem_u32(&sff[0]), 0, wc, kSiteMmaScale)) goto mma_done_r;
+        taken = 1;  // the scale writers saw full[0]
+        tc_fence_after();
+        for (int i = 0; i < nst; ++i) {
+          if (i > 0) {
+            if (!mbar_wait(smem_u32(&full[i]), 0, wc, kSiteMmaFull)) goto mma_done_r;
+            taken = i + 1;
+          }
+          const uint32_t slot = tmem + C::SF_COL0 + i * C::SF_SLOT;
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(smem + i * C::A_BYTES));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + C::B_REGION + i * C::B_BYTES));
+          const uint32_t sb = slot + C::SFA_COLS;
+          constexpr uint32_t SB = 4 * C::SFB_BLOCKS;
+          if constexpr (!C::MX) {
+            mma_nvf4(tmem, adesc, bdesc, C::IDESC, slot, sb, i > 0 ? 1u : 0u);
+            mma_nvf4(tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
+            mma_nvf4(tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
+            mma_nvf4(tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
+          }
+        }
+        tc_commit(smem_u32(&accf[0]));
+      }
+    mma_done_r:
+      *consumed = taken;
+    } else if (lane == 0) {
       int stage = 0;
       int taken = 0;  // stages known landed (abort drain)
       int acc = 0;
@@ -531,9 +627,9 @@ __global__ void __launch_bounds__(320, 1)
           if (!mbar_wait(smem_u32(&sff[s_idx]), s_round & 1, wc, kSiteMmaScale)) goto mma_done;
           ++taken;
           tc_fence_after();
-          const uint8_t *st = smem + stage * C::STAGE_BYTES;
           const uint32_t slot = tmem + C::SF_COL0 + s_idx * C::SF_SLOT;
-          const uint64_t adesc = sdesc_k_sw128(smem_u32(st)), bdesc = sdesc_k_sw128(smem_u32(st + C::A_BYTES));
+          const uint64_t adesc = sdesc_k_sw128(smem_u32(smem + stage * C::A_BYTES));
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + C::B_REGION + stage * C::B_BYTES));
           const uint32_t acc0 = kt > sg.kt0 ? 1u : 0u;
           if constexpr (C::MX) {
             // MXFP4: a 512-byte scale chunk covers 128 K elements = two MMAs (scale ids 0, 2)
@@ -587,13 +683,50 @@ __global__ void __launch_bounds__(320, 1)
     uint32_t phase = 0;
     uint32_t it = 0;
     Work w = work0;
+    if (!GROUPED && p.resident) {
+      // Resident slice: all scale slices landed with stage 0; fill every stage's slot, then
+      // hand the slots to the MMA lane with a single arrival.
+      Seg sg;
+      if (w.next(p, sg)) {
+        if (!mbar_wait(smem_u32(&full[0]), 0, wc, kSiteScaleFull)) goto scale_done;
+        for (int i = 0; i < sg.kt1 - sg.kt0; ++i) {
+          const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + i * C::SFA_BYTES);
+          const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + i * C::SFB_BYTES);
+          uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
+#pragma unroll
+          for (int c = 0; c < C::CHUNKS; ++c) {
+            const uint4 v = lds128(sfa_s + 512 * c + 16 * lane);
+            ra[4 * c] = v.x;
+            ra[4 * c + 1] = v.y;
+            ra[4 * c + 2] = v.z;
+            ra[4 * c + 3] = v.w;
+#pragma unroll
+            for (int b = 0; b < C::SFB_BLOCKS; ++b) {
+              const uint4 u = lds128(sfb_s + (b * C::CHUNKS + c) * 512 + 16 * lane);
+              const int o = c * 4 * C::SFB_BLOCKS + 4 * b;
+              rb[o] = u.x;
+              rb[o + 1] = u.y;
+              rb[o + 2] = u.z;
+              rb[o + 3] = u.w;
+            }
+          }
+          const uint32_t slot = tmem + lane_base + C::SF_COL0 + i * C::SF_SLOT;
+          tmem_st_32x32b<C::SFA_COLS>(slot, ra);
+          tmem_st_32x32b<C::SFB_COLS>(slot + C::SFA_COLS, rb);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sff[0]));
+      }
+    } else
     for (Seg sg; w.next(p, sg);) {
       for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
         const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
         if (!mbar_wait(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc, kSiteScaleSlot)) goto scale_done;
         if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
-        const uint32_t sfa_s = smem_u32(smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES);
-        const uint32_t sfb_s = sfa_s + C::SFA_BYTES;
+        const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + stage * C::SFA_BYTES);
+        const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + stage * C::SFB_BYTES);
         uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
@@ -632,7 +765,28 @@ __global__ void __launch_bounds__(320, 1)
     const int quad = warp & 3;  // tcgen05.ld: warp w reaches lanes 32*(w%4) .. +31
     const int row = quad * 32 + lane;
     const int tid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
-    const float alpha = p.alpha ? *p.alpha : 1.0f;
+    // alpha is read by one thread and shared: a load left to each thread's first use was
+    // scheduled there, putting a full memory latency (~1400 cycles) in front of the stores.
+    if (tid == 0) *alpha_s = p.alpha ? *p.alpha : 1.0f;
+    {
+      // Touch the output lines of this CTA's first tile now: the first store to a cold page
+      // otherwise waits for its address translation at the very end of the kernel.
+      Work w = work0;
+      Seg sg{};
+      if (w.next(p, sg)) {
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+        if (row < t.rows) {
+          if (p.swap) {
+            prefetch_l2(p.d + t.out_j0 * p.ldd + t.out_i0 + row);
+            prefetch_l2(p.d + (t.out_j0 + t.cols - 1) * p.ldd + t.out_i0 + row);
+          } else {
+            prefetch_l2(p.d + (t.out_i0 + row) * p.ldd + t.out_j0);
+          }
+        }
+      }
+    }
+    named_barrier_sync(2, 128);
+    const float alpha = *alpha_s;
     int acc = 0;
     uint32_t acc_phase = 0;
     Work w = work0;

@@ -80,6 +80,6 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
   const int64_t max_tiles = (ceil_div(t, 128) + num_experts) * args.n_tiles;
   const int grid = static_cast<int>(max_tiles < dev.sm_count ? max_tiles : dev.sm_count);
   cudaError_t e = launch(kern, dim3(grid), dim3(GroupedCfg::THREADS), GroupedCfg::smem_bytes(true), (cudaStream_t)stream,
-                         (flags & NVFP4_FLAG_PDL) != 0, 1, ta, tb, args);
+                         (flags & NVFP4_FLAG_PDL) != 0, 1, ta, tb, tb, args);
   return check_launch(e, "mxfp4_grouped_gemm");
 }

@@ -32,6 +32,13 @@ nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t in
                                  uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
                                  uint32_t box_rows, bool swizzle128);
 
+// 3-D view of a K-major FP4 operand [rows, K/2 bytes] for loading a run of K stages in one copy:
+// dims {128 bytes, rows, K/256 stages}, strides {row stride, 128}, box {128, box_rows, box_stages},
+// 128-byte swizzle.  The box lands as box_stages consecutive (box_rows x 128-byte) tiles.
+// Needs K % 256 == 0 (otherwise the last stage would run into the next row).
+nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_t k_bytes, uint64_t rows,
+                                     uint32_t box_rows, uint32_t box_stages);
+
 // Raises the dynamic shared-memory limit of `fn` on the current device (once per device).
 nvfp4_status_t allow_smem(const void *fn, int bytes, int device);
 

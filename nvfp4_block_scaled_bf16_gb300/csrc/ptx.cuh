@@ -38,6 +38,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps until the phase
+// completes or `ns` nanoseconds pass, instead of returning at once.  Polling without the hint
+// keeps the shared-memory pipe busy with barrier tests, which the producer's own barrier and
+// copy instructions then queue behind.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after `limit` SM clock cycles (or as soon as another role of the
 // CTA has given up), records the time-out in the device status word and returns false.
 struct WaitCtl {
@@ -45,12 +60,15 @@ struct WaitCtl {
   volatile int *abort;     // shared-memory flag: some role of this CTA gave up
   unsigned int *status;    // device status word read by nvfp4_check_status
 };
+// Sleep bound of one test inside a bounded wait (ns): the abort flag and the clock are checked
+// at least this often.
+constexpr uint32_t kWaitSleepNs = 200000;
 // Bounded wait; on expiry sets bit 0 of the status word and bit 8 + site (which wait gave up).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w, int site) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*w.abort) return false;
     if (clock64() - t0 > w.limit) {
       *w.abort = 1;
@@ -72,6 +90,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
+// 3-D tensor box -> shared memory; the box lands as box[2] consecutive (box[1] x box[0]) tiles.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 // Prefetch one TMA box of a tensor map into L2 (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
@@ -82,6 +109,11 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
 // Prefetch a contiguous range into L2; address 16-B aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+// Brings the line holding `p` into L2 (and its address translation into the TLBs) ahead of
+// the stores that will write it.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 // Contiguous global -> shared copy; src/dst 16-B aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
