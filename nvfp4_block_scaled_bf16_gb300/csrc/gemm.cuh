@@ -916,48 +916,59 @@ __global__ void __launch_bounds__(320, 1)
   if constexpr (!GROUPED) {
     if (p.splits > 1) {
       // Split-K reduction across the cluster.  The partial tile is stored column-major
-      // (128 rows per column); CTA `rank` owns a contiguous 1/splits of its 4-row groups.  Each
-      // thread first issues the loads of every rank's partial (independent, so their latencies
-      // overlap), then sums them in rank order (fixed order: deterministic output).
+      // (128 rows per column, a 4-row group per float4 unit); only the units of the tile's
+      // valid columns are reduced, CTA `rank` taking a contiguous 1/splits of them.  Every
+      // thread of the CTA takes part, two units at a time: it issues the loads of every rank's
+      // partial for both (independent, so their latencies overlap), then sums each in rank
+      // order (a fixed order: deterministic output).
       cluster_sync();
-      if (warp >= 2 && warp < 6) {
-        const int tid = threadIdx.x - 64;  // 0..127
+      {
         const int rank = static_cast<int>(cluster_ctarank());
         Work w = work0;
         Seg sg{};
         w.next(p, sg);
         const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
-        const float alpha = p.alpha ? *p.alpha : 1.0f;
-        constexpr int UNITS = C::BN * 128 / 4;  // float4 groups in the tile
-        const int u0 = rank * UNITS / p.splits, u1 = (rank + 1) * UNITS / p.splits;
+        const float alpha = *alpha_s;
+        const int units = min(t.cols, C::BN) * 32;  // float4 groups of the valid columns
+        const int u0 = rank * units / p.splits, u1 = (rank + 1) * units / p.splits;
         const uint32_t red0 = smem_u32(smem);
-        for (int u = u0 + tid; u < u1; u += 128) {
-          const uint32_t off = red0 + static_cast<uint32_t>(u * 16);
-          float4 part[8];
+        constexpr int NT = C::THREADS;
+        for (int ub = u0 + static_cast<int>(threadIdx.x); ub < u1; ub += 2 * NT) {
+          float4 part[2][8];
 #pragma unroll
-          for (int s = 0; s < 8; ++s)
-            if (s < p.splits) part[s] = ld_cluster_v4(map_to_rank(off, s));
-          float4 v = part[0];
+          for (int h = 0; h < 2; ++h) {
+            const int u = ub + h * NT;
+            const uint32_t off = red0 + static_cast<uint32_t>((u < u1 ? u : ub) * 16);
 #pragma unroll
-          for (int s = 1; s < 8; ++s)
-            if (s < p.splits) {
-              v.x += part[s].x;
-              v.y += part[s].y;
-              v.z += part[s].z;
-              v.w += part[s].w;
-            }
-          const int c = (u * 4) / 128, r0 = (u * 4) % 128;
-          if (r0 < t.rows && c < t.cols) {
-            const float o[4] = {v.x, v.y, v.z, v.w};
-            if (p.swap) {
-              uint2 pk;
-              pk.x = pack_bf16x2(__fmul_rn(alpha, o[0]), __fmul_rn(alpha, o[1]));
-              pk.y = pack_bf16x2(__fmul_rn(alpha, o[2]), __fmul_rn(alpha, o[3]));
-              *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
-            } else {
+            for (int s = 0; s < 8; ++s)
+              if (s < p.splits) part[h][s] = ld_cluster_v4(map_to_rank(off, s));
+          }
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                p.d[(t.out_i0 + r0 + i) * p.ldd + t.out_j0 + c] = __float2bfloat16_rn(__fmul_rn(alpha, o[i]));
+          for (int h = 0; h < 2; ++h) {
+            const int u = ub + h * NT;
+            if (u >= u1) break;
+            float4 v = part[h][0];
+#pragma unroll
+            for (int s = 1; s < 8; ++s)
+              if (s < p.splits) {
+                v.x += part[h][s].x;
+                v.y += part[h][s].y;
+                v.z += part[h][s].z;
+                v.w += part[h][s].w;
+              }
+            const int c = (u * 4) / 128, r0 = (u * 4) % 128;
+            if (r0 < t.rows) {
+              const float o[4] = {v.x, v.y, v.z, v.w};
+              if (p.swap) {
+                uint2 pk;
+                pk.x = pack_bf16x2(__fmul_rn(alpha, o[0]), __fmul_rn(alpha, o[1]));
+                pk.y = pack_bf16x2(__fmul_rn(alpha, o[2]), __fmul_rn(alpha, o[3]));
+                *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
+              } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  p.d[(t.out_i0 + r0 + i) * p.ldd + t.out_j0 + c] = __float2bfloat16_rn(__fmul_rn(alpha, o[i]));
+              }
             }
           }
         }
