@@ -92,9 +92,12 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     pl.ws_bytes = round_up(static_cast<int64_t>(pl.sk_tiles) * 4, kWsAlign) +
                   static_cast<size_t>(pl.ctas) * 2 * 128 * pl.bn * 4;
   // Rings as deep as shared memory allows: a swap-AB CTA then has its whole K run in flight
-  // from the start (the decode GEMM is bound by load latency, not by shared memory).
+  // from the start (the decode GEMM is bound by load latency, not by shared memory).  The
+  // narrowest tiles instead keep a 4-stage ring so that two CTAs fit an SM: under PDL the next
+  // GEMM's CTAs then start beside this one's and pull their weights (ring + L2 prefetch) while
+  // this one finishes.
   switch (pl.bn) {
-    case 32: pl.stages = 8; break;
+    case 32: pl.stages = 4; break;
     case 64: pl.stages = 7; break;
     case 128: pl.stages = 6; break;
     default: pl.stages = 4; break;
@@ -106,7 +109,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   // Weight-streaming (swap-AB) CTAs keep only a few stages in flight: when every CTA requests
   // its whole slice at once, cold HBM completes all of a CTA's stages at about the same time and
   // the MMAs cannot overlap the loads; paced requests land in order.
-  pl.lookahead = pl.swap ? 3 : 0;
+  pl.lookahead = pl.swap && pl.bn > 32 ? 3 : 0;
   return pl;
 }
 
@@ -125,7 +128,7 @@ nvfp4_status_t with_config(const Plan &pl, F &&f) {
   // swap-AB CTAs hold one tile (single accumulator); large-M CTAs walk tiles persistently and
   // overlap the epilogue with the next tile where tensor memory allows
   switch (pl.bn) {
-    case 32: return f(GemmCfg<32, 8, false, false>{});
+    case 32: return f(GemmCfg<32, 4, false, false, 2>{});
     case 64: return f(GemmCfg<64, 7, false, false>{});
     case 128: return pl.swap ? f(GemmCfg<128, 6, false, false>{}) : f(GemmCfg<128, 6, false, true>{});
     default: return pl.swap ? f(GemmCfg<256, 4, false, false>{}) : f(GemmCfg<256, 4, false, true>{});

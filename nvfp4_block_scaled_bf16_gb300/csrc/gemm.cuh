@@ -60,11 +60,18 @@ enum : int {
   kSiteEpilogue = 6     // epilogue: accumulator complete
 };
 
-template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true>
+template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
   static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
   static constexpr bool MX = MX_;         // true: MXFP4 (ue8m0 / 32); false: NVFP4 (ue4m3 / 16)
+  // MULTI_TILE: CTAs walk several tiles (whole tiles or stream-K; never swap-AB).  Otherwise the
+  // configuration serves swap-AB plans only: one tile per CTA, K split over a cluster.
+  static constexpr bool MULTI_TILE = MULTI_TILE_;
+  static constexpr bool SWAP_ONLY = !MULTI_TILE_;
+  // CTAs per SM the registers are budgeted for (2: consecutive GEMMs of a PDL chain can share
+  // the SMs, the next one streaming its weights while this one finishes)
+  static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
   static constexpr int BM = 128;          // MMA M: rows of operand A per tile
   static constexpr int KSTAGE = 256;      // K elements per stage = one 128-byte TMA row
   static constexpr int VEC = MX ? 32 : 16;
@@ -107,6 +114,8 @@ struct GemmCfg {
   static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8, "tensor memory budget, scale-slot barriers");
   static_assert((2 * STAGES + 22) * 8 + 7 * 4 <= CTRL_BYTES, "barriers and flags fit the control block");
   static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
+  static_assert(MIN_BLOCKS == 1 || (MIN_BLOCKS * (smem_bytes(false) + 1024) <= 233472 && MIN_BLOCKS * TMEM_COLS <= 512),
+                "shared and tensor memory for MIN_BLOCKS CTAs per SM");
   static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
@@ -379,7 +388,7 @@ __device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, c
 }
 
 template <class C, bool GROUPED>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -543,6 +552,14 @@ __global__ void __launch_bounds__(320, 1)
             const int nch = stage_chunks<C>(p, kt);
             mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
             if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
+          }
+          if (C::SWAP_ONLY && pre_a) {
+            // The rest of this CTA's weight slice goes to L2 now, while the preceding kernel runs;
+            // the ring then refills from L2 instead of from cold HBM.
+            for (int kt = s0.kt0 + pre; kt < s0.kt1; ++kt) tma_prefetch_l2_2d(&tmA, kt * 128, t.a_y);
+            if (s0.kt0 + pre < s0.kt1)
+              bulk_prefetch_l2(t.sfa_blk + static_cast<int64_t>(s0.kt0 + pre) * C::CHUNKS * 512,
+                               (s0.kt1 - s0.kt0 - pre) * C::CHUNKS * 512);
           }
         }
         pdl_wait();
@@ -796,7 +813,7 @@ __global__ void __launch_bounds__(320, 1)
     // wait returns at once), so all four always meet the same named barriers.
     for (Seg sg; w.next(p, sg);) {
       const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
-      const bool sk_part = !GROUPED && p.splits == 1 && sg.n > 1;
+      const bool sk_part = C::MULTI_TILE && !GROUPED && p.splits == 1 && sg.n > 1;
       const bool ok = mbar_wait(smem_u32(&accf[acc]), acc_phase, wc, kSiteEpilogue);
       tc_fence_after();
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
@@ -807,7 +824,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_base + 32 * c, r);
         tmem_ld_wait();
-        if (p.splits > 1) {
+        if (C::SWAP_ONLY && p.splits > 1) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
         } else if (sk_part) {
@@ -819,7 +836,7 @@ __global__ void __launch_bounds__(320, 1)
             for (int i = 0; i < 8; ++i) v[i] = r[8 * q + i];
             st_global_v8(dst + 8 * q, v);
           }
-        } else if (!p.swap) {
+        } else if (!C::SWAP_ONLY) {
           if (row < t.rows && 32 * c < t.cols) {
             __nv_bfloat16 *out = p.d + (t.out_i0 + row) * p.ldd + t.out_j0 + 32 * c;
 #pragma unroll
@@ -913,7 +930,7 @@ __global__ void __launch_bounds__(320, 1)
     __syncthreads();
   }
 
-  if constexpr (!GROUPED) {
+  if constexpr (!GROUPED && C::SWAP_ONLY) {
     if (p.splits > 1) {
       // Split-K reduction across the cluster.  The partial tile is stored column-major
       // (128 rows per column, a 4-row group per float4 unit); only the units of the tile's
