@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the NVFP4 quantise -> GEMM hot path on one GB300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|e2e|moe]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|e2e|moe|pipeline]
     python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
 
 Workloads (synthetic, seeded; shapes and value distributions of the pages' benchmarks):
@@ -16,6 +16,9 @@ Workloads (synthetic, seeded; shapes and value distributions of the pages' bench
   moe                 MXFP4: 4096 tokens top-8 over 128 experts (32768 rows); quantise, then the
                       gate+up grouped GEMM (N=1536, K=2048) and the down grouped GEMM (N=2048,
                       K=768) on a second quantised activation.
+  pipeline            4 back-to-back quant->GEMM layers (N=K=7168, own weight per layer) at
+                      M in {1,16,64,256,1024,2048,4096}; the line adds each M's 4-layer time
+                      with and without PDL.
 Each step is captured once in a CUDA graph and replayed; the L2 is flushed before every timed
 step, outside the timed interval: a 512 MB write, then a 512 MB read of a second buffer, so the
 step starts with none of its inputs in L2 and with L2 holding clean lines (as after the previous
@@ -168,7 +171,7 @@ def _gs(x: torch.Tensor) -> float:
 
 def build_nvfp4_chain(nv, wl: Workload, shapes, weight_seed=0, weights_by_shape=None, pdl=True):
     flags = nv.FLAG_PDL if pdl else 0
-    cache = {}
+    cache = {} if weights_by_shape is None else weights_by_shape
     # one zeroed split-K workspace serves every GEMM of the chain (they run in stream order)
     ws = nv.gemm_workspace(max(nv.gemm_workspace_size(m, n, k) for (m, n, k) in shapes))
     for i, (m, n, k) in enumerate(shapes):
@@ -269,6 +272,30 @@ def make_moe(nv):
     return wl
 
 
+PIPE_MS = (1, 16, 64, 256, 1024, 2048, 4096)
+PIPE_LAYERS = 4
+
+
+def pipeline_shapes(m):
+    return [(m, 7168, 7168)] * PIPE_LAYERS
+
+
+def make_pipeline(nv):
+    """Back-to-back quant->GEMM layers (vLLM fork compare view "add pdl",
+    benchmark_nvfp4_sm103.py, benchmark_pdl_pipeline: 4 layers, N = K = 7168).  One step runs
+    the 4-layer pipeline at every M of PIPE_MS; each layer streams its own weight copy (the page
+    reuses one weight for all layers, which L2 would then hold after the first)."""
+    wl = Workload(nv, "pipeline")
+    cache = {}
+    build_nvfp4_chain(nv, wl, [s for m in PIPE_MS for s in pipeline_shapes(m)], weights_by_shape=cache)
+    wl.extra["weights"] = cache
+    wl.config = {"workload": f"{PIPE_LAYERS}-layer quant->GEMM pipeline with PDL, N=K=7168, M in {','.join(map(str, PIPE_MS))}",
+                 "global_batch": PIPE_LAYERS * sum(PIPE_MS), "layers": PIPE_LAYERS, "n": 7168, "k": 7168,
+                 "inputs": "activation N(0,1) with 0.1% outlier channels x20, weight N(0,0.02), seed 0",
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
+    return wl
+
+
 def make_custom(nv, shapes):
     wl = Workload(nv, "custom")
     build_nvfp4_chain(nv, wl, shapes)
@@ -277,7 +304,7 @@ def make_custom(nv, shapes):
     return wl
 
 
-MAKERS = {"decode": make_decode, "prefill": make_prefill, "e2e": make_e2e, "moe": make_moe}
+MAKERS = {"decode": make_decode, "prefill": make_prefill, "e2e": make_e2e, "moe": make_moe, "pipeline": make_pipeline}
 
 
 # ---------------------------------------------------------------------------- timing
@@ -436,6 +463,24 @@ def run_ours(args, dist_on, rank, world):
             g2.replay()
         t2 = timed_replays(g2, args.steps, flush)
         line["without_pdl_ms_per_step"] = round(max_over_ranks(statistics.mean(t2), dist_on), 5)
+    if wl.name == "pipeline":
+        # per M: the 4-layer pipeline alone, with and without PDL (the page's table)
+        per_m = {}
+        for m in PIPE_MS:
+            row = {}
+            for tag, pdl in (("pdl_us", True), ("no_pdl_us", False)):
+                w_m = Workload(nv, "pipeline_m")
+                build_nvfp4_chain(nv, w_m, pipeline_shapes(m), weights_by_shape=wl.extra["weights"], pdl=pdl)
+                g_m = capture(w_m.launches)
+                for _ in range(args.warmup):
+                    g_m.replay()
+                t_m = statistics.mean(timed_replays(g_m, max(3, min(args.steps, 50)), flush)) * 1e3
+                row[tag] = round(max_over_ranks(t_m, dist_on), 2)
+                del g_m, w_m
+            row["pdl_tflops"] = round(2.0 * m * 7168 * 7168 * PIPE_LAYERS / (row["pdl_us"] * 1e-6) / 1e12, 2)
+            row["pdl_speedup"] = round(row["no_pdl_us"] / row["pdl_us"], 3)
+            per_m[str(m)] = row
+        line["pipeline"] = per_m
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(args.workload)
         print(json.dumps(line), flush=True)
@@ -463,6 +508,9 @@ def oracle_step(workload: str, n_rows_sample: int):
     elif workload == "e2e":
         shapes = [(m, n_rows_sample, 4096) for m in (256, 512)]
         desc = f"both e2e M, {n_rows_sample} of 14336 weight rows"
+    elif workload == "pipeline":
+        shapes = [(min(m, 64), n_rows_sample, 7168) for m in PIPE_MS]
+        desc = f"one layer per pipeline M (at most 64 activation rows), {n_rows_sample} of 7168 weight rows, K=7168"
     else:
         shapes = [(m, n_rows_sample, 7168) for m in DECODE_MS]
         desc = f"all 8 decode M, {n_rows_sample} of 4096 weight rows, K=7168"
