@@ -65,6 +65,13 @@ enum {
    * [vLLM-SM103] summary.md "What is PDL?", nvfp4_quant_kernels.cu "Host entry: SM103
    * activation quantization" (use_pdl). */
   NVFP4_FLAG_PDL = 1u << 0,
+  /* Scale buffers in the SM103 layout instead of the 128x4 ("SM100") one: nvfp4_quantize writes
+   * its scales, nvfp4_gemm / nvfp4_gemm_noalloc read both sfa and sfb, in that layout.  Same
+   * 512-byte tiles in the same order; inside a tile, row m = m4b + 4*m4a + 16*m8 and scale
+   * column k sit at m8*16 + m4a*128 + m4b*4 + k.  [vLLM-SM103] nvfp4_quant_kernels.cu "Scale
+   * factor layout conversion: SM100 <-> SM103", nvfp4_utils.cuh (SM103 swizzled SF offset).
+   * Not accepted by the MXFP4 entry points. */
+  NVFP4_FLAG_SF_SM103 = 1u << 2,
   /* Short (about 20 ms) limit on every pipeline wait instead of the default (about 10 s);
    * for tests of the timeout path. */
   NVFP4_FLAG_DEBUG_TIMEOUT = 1u << 8,
@@ -220,6 +227,19 @@ nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const in
  * Buffers must not overlap.  No alignment requirement. */
 nvfp4_status_t sf_swizzle(const uint8_t *src, uint8_t *dst, int64_t rows, int64_t cols,
                           int to_swizzled, nvfp4_stream_t stream);
+
+/* Converts a swizzled NVFP4 scale buffer between the 128x4 ("SM100") layout and the SM103
+ * layout (see NVFP4_FLAG_SF_SM103): every byte of every 512-byte tile moves to its place in the
+ * other layout, padding bytes included.
+ * Source: [vLLM-SM103] nvfp4_quant_kernels.cu "Scale factor layout conversion: SM100 <-> SM103"
+ * (convert_sf_layout_sm100_to_sm103 / _sm103_to_sm100).
+ *   src, dst   uint8 [round_up(rows,128) * round_up(cols,4)], 16-B aligned, must not overlap
+ *   rows, cols the scale matrix (cols = K/16 scale columns)
+ *   to_sm103   1: SM100 -> SM103, 0: SM103 -> SM100
+ * Reads src only after the PDL wait (NVFP4_FLAG_PDL semantics are implied: the kernel always
+ * waits, so it is safe after any producer). */
+nvfp4_status_t nvfp4_sf_convert_layout(const uint8_t *src, uint8_t *dst, int64_t rows, int64_t cols,
+                                       int to_sm103, nvfp4_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that kernels set when a
  * bounded pipeline wait gave up or a grouped GEMM found malformed row offsets.  Returns

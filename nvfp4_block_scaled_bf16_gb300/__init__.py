@@ -21,6 +21,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 _i64, _u32, _int, _vp, _sz = ctypes.c_int64, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
 
 FLAG_PDL = 1 << 0
+FLAG_SF_SM103 = 1 << 2
 FLAG_DEBUG_TIMEOUT = 1 << 8
 FLAG_DEBUG_SKIP_FIRST_LOAD = 1 << 9
 
@@ -46,6 +47,7 @@ _SIGS = {
     "nvfp4_gemm_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
+    "nvfp4_sf_convert_layout": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_check_status": (_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -248,6 +250,15 @@ def sf_swizzle(src, rows: int, cols: int, to_swizzled: bool = True, dst=None, st
         n = (-(-rows // 128) * 128) * (-(-cols // 4) * 4) if to_swizzled else rows * cols
         dst = torch.empty(n, dtype=torch.uint8, device=src.device)
     _check(_lib.sf_swizzle(_ptr(src), _ptr(dst), rows, cols, 1 if to_swizzled else 0, _stream(stream)))
+    return dst
+
+
+def sf_convert_layout(src, rows: int, cols: int, to_sm103: bool = True, dst=None, stream=None):
+    """Swizzled NVFP4 scale buffer: 128x4 ("SM100") layout <-> SM103 layout."""
+    _need(src, torch.uint8, "src")
+    if dst is None:
+        dst = torch.empty_like(src)
+    _check(_lib.nvfp4_sf_convert_layout(_ptr(src), _ptr(dst), rows, cols, 1 if to_sm103 else 0, _stream(stream)))
     return dst
 
 

@@ -177,7 +177,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: m=%lld n=%lld k=%lld", (long long)m, (long long)n, (long long)k);
   if (k % 32 || n % 32)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_gemm: need k %% 32 == 0 and n %% 32 == 0 (k=%lld n=%lld)", (long long)k, (long long)n);
-  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD))
+  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD | NVFP4_FLAG_SF_SM103))
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: unknown flags 0x%x", flags);
   if (m == 0) return NVFP4_OK;
   if (!a || !sfa || !b || !sfb || !alpha || !d) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: null pointer");
@@ -237,6 +237,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.resident = pl.resident;
   args.nst_max = pl.nst_max;
   args.lookahead = pl.lookahead;
+  args.sf_sm103 = (flags & NVFP4_FLAG_SF_SM103) ? 1 : 0;
   if (pl.sk_tiles > 0) {
     args.ws_cnt = static_cast<unsigned int *>(workspace);
     args.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +

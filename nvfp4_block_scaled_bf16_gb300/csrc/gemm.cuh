@@ -149,7 +149,22 @@ struct GemmArgs {
   int nst_max;                // resident: K stages of the longest slice = z extent of tmB3's box
   int lookahead;              // > 0: at most this many K stages in flight per CTA (stage i + L is
                               // issued once stage i has landed); 0: as many as the ring holds
+  int sf_sm103;               // 1: both scale buffers are in the SM103 layout
 };
+
+// The 16 scale bytes of 512-byte scale tile `tile` that lane i of a scale writer puts in its
+// tensor-memory lane: rows i, i+32, i+64, i+96 (4 consecutive bytes each, one per scale column).
+// In the 128x4 layout those are bytes 16i .. 16i+15; in the SM103 layout the word of row m sits
+// at ((m/16)%8)*16 + ((m/4)%4)*128 + (m%4)*4, which for m = i + 32q is base(i) + 32q.
+__device__ __forceinline__ uint4 ld_sf_lane(uint32_t tile, int lane, int sm103) {
+  if (!sm103) return lds128(tile + 16 * lane);
+  const uint32_t base = tile + ((lane >> 4) * 16 + ((lane >> 2) & 3) * 128 + (lane & 3) * 4);
+  uint4 v;
+  asm volatile("ld.shared.b32 %0, [%4];\n ld.shared.b32 %1, [%4+32];\n ld.shared.b32 %2, [%4+64];\n ld.shared.b32 %3, [%4+96];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(base));
+  return v;
+}
 
 struct TileInfo {
   int a_y, b_y;                // TMA row coordinates of the A and B tiles
@@ -712,14 +727,14 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
           uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c) {
-            const uint4 v = lds128(sfa_s + 512 * c + 16 * lane);
+            const uint4 v = ld_sf_lane(sfa_s + 512 * c, lane, p.sf_sm103);
             ra[4 * c] = v.x;
             ra[4 * c + 1] = v.y;
             ra[4 * c + 2] = v.z;
             ra[4 * c + 3] = v.w;
 #pragma unroll
             for (int b = 0; b < C::SFB_BLOCKS; ++b) {
-              const uint4 u = lds128(sfb_s + (b * C::CHUNKS + c) * 512 + 16 * lane);
+              const uint4 u = ld_sf_lane(sfb_s + (b * C::CHUNKS + c) * 512, lane, p.sf_sm103);
               const int o = c * 4 * C::SFB_BLOCKS + 4 * b;
               rb[o] = u.x;
               rb[o + 1] = u.y;
@@ -747,14 +762,14 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
-          const uint4 v = lds128(sfa_s + 512 * c + 16 * lane);
+          const uint4 v = ld_sf_lane(sfa_s + 512 * c, lane, p.sf_sm103);
           ra[4 * c] = v.x;
           ra[4 * c + 1] = v.y;
           ra[4 * c + 2] = v.z;
           ra[4 * c + 3] = v.w;
 #pragma unroll
           for (int b = 0; b < C::SFB_BLOCKS; ++b) {
-            const uint4 w = lds128(sfb_s + (b * C::CHUNKS + c) * 512 + 16 * lane);
+            const uint4 w = ld_sf_lane(sfb_s + (b * C::CHUNKS + c) * 512, lane, p.sf_sm103);
             const int o = c * 4 * C::SFB_BLOCKS + 4 * b;
             rb[o] = w.x;
             rb[o + 1] = w.y;

@@ -65,7 +65,7 @@ extern "C" nvfp4_status_t nvfp4_gemm_noalloc(const uint8_t *a, const uint8_t *sf
     return nvfp4_gemm(a, sfa, b, sfb, alpha, d, m, n, k, nullptr, 0, flags, stream);
   if (!a || !sfa || !b || !sfb || !alpha || !d || !nvfp4::aligned(a, 32) || !nvfp4::aligned(b, 32) ||
       !nvfp4::aligned(d, 32) || !nvfp4::aligned(sfa, 16) || !nvfp4::aligned(sfb, 16) || !nvfp4::aligned(alpha, 4) ||
-      (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD)))
+      (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD | NVFP4_FLAG_SF_SM103)))
     return nvfp4_gemm(a, sfa, b, sfb, alpha, d, m, n, k, nullptr, 0, flags, stream);
   nvfp4::DeviceInfo dev;
   nvfp4_status_t st = nvfp4::current_device(&dev);

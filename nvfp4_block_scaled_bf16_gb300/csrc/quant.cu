@@ -22,6 +22,13 @@ namespace {
 __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t j, int64_t cp) {
   return ((r >> 7) * (cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
+// The SM103 layout (same tiles; inside a tile row m = m4b + 4*m4a + 16*m8 sits at
+// m8*16 + m4a*128 + m4b*4): vLLM fork compare view "add pdl", nvfp4_utils.cuh, SM103 swizzled
+// SF offset, written by that page's SM103 quantisation kernel.
+__device__ __forceinline__ int64_t sf_offset_sm103(int64_t r, int64_t j, int64_t cp) {
+  const int64_t m = r & 127;
+  return ((r >> 7) * (cp >> 2) + (j >> 2)) * 512 + ((m >> 4) & 7) * 16 + ((m >> 2) & 3) * 128 + (m & 3) * 4 + (j & 3);
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float *f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -41,6 +48,8 @@ __device__ __forceinline__ uint32_t gather4(uint32_t code) {
 }
 
 // total = round_up(m,128) * cp, a multiple of 512, so every warp runs the same trip count.
+// SM103: scales in the SM103 layout instead of the 128x4 one.
+template <bool SM103>
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                           int64_t m, int64_t kb, int64_t ldx,
                                                           const float *__restrict__ gs_ptr,
@@ -82,7 +91,7 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *_
       *reinterpret_cast<uint2 *>(q + r * (kb * 8) + j * 8) = out;
     }
     const uint32_t word = gather4(code);
-    if ((j & 3) == 0) *reinterpret_cast<uint32_t *>(sf + sf_offset(r, j, cp)) = word;
+    if ((j & 3) == 0) *reinterpret_cast<uint32_t *>(sf + (SM103 ? sf_offset_sm103(r, j, cp) : sf_offset(r, j, cp))) = word;
   }
 }
 
@@ -190,7 +199,7 @@ extern "C" nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, in
   if (!x || !gs || !q || !sf) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize: null pointer");
   if (!aligned(x, 16) || !aligned(q, 8) || !aligned(sf, 16) || !aligned(gs, 4))
     return fail(NVFP4_ERR_MISALIGNED, "nvfp4_quantize: x needs 16-B, q 8-B, sf 16-B, gs 4-B alignment");
-  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT))
+  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_SF_SM103))
     return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize: unknown flags 0x%x", flags);
   DeviceInfo dev;
   nvfp4_status_t st = current_device(&dev);
@@ -198,7 +207,8 @@ extern "C" nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, in
   const int64_t cp = round_up(k / 16, 4);
   const int64_t total = round_up(m, 128) * cp;
   const int grid = quant_grid(total, dev.sm_count);
-  cudaError_t e = launch(nvfp4_quant_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+  auto kern = (flags & NVFP4_FLAG_SF_SM103) ? nvfp4_quant_kernel<true> : nvfp4_quant_kernel<false>;
+  cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, m, k / 16,
                          ldx, gs, q, sf, total, cp);
   return check_launch(e, "nvfp4_quantize");

@@ -123,3 +123,17 @@ def test_quantizers_reject_bad_arguments_without_a_device(lib):
     assert L.mxfp4_grouped_gemm(_c(X), _c(S), _c(X), 0, _c(X), _c(S), None, _c(Q), 4, 64, 64, 0, None) == 1
     assert L.sf_swizzle(_c(X), _c(Q), -1, 4, 1, None) == 1
     assert L.sf_swizzle(_c(X), _c(Q), 4, 4, 7, None) == 1
+
+
+def test_layout_conversion_rejects_bad_arguments_without_a_device(lib):
+    L = lib.lib
+    S, D = 0x10000, 0x90000
+    assert L.nvfp4_sf_convert_layout(_c(S), _c(D), -1, 4, 1, None) == 1
+    assert L.nvfp4_sf_convert_layout(_c(S), _c(D), 4, 4, 2, None) == 1          # direction
+    assert L.nvfp4_sf_convert_layout(None, _c(D), 4, 4, 1, None) == 1
+    assert L.nvfp4_sf_convert_layout(_c(S + 4), _c(D), 4, 4, 1, None) == 2      # alignment
+    assert L.nvfp4_sf_convert_layout(_c(S), _c(S + 256), 4, 4, 1, None) == 1    # overlap (512 B)
+    assert L.nvfp4_sf_convert_layout(None, None, 0, 4, 1, None) == 0            # empty: no-op
+    # the SM103 layout is an NVFP4 layout: the MXFP4 entry points refuse the flag
+    X, Q = 0x10000, 0x30000
+    assert L.mxfp4_quantize(_c(X), 4, 64, 64, None, 0, _c(Q), _c(S), 1 << 20, lib.FLAG_SF_SM103, None) == 1
