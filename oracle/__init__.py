@@ -25,4 +25,4 @@ quantiser operation order, sign of zero for e2m1, nibble order, e4m3
 saturation and the MXFP4 scale rounding (round up to a power of two).
 Parity pins: every function here is pinned by tests/test_oracle_*.py.
 """
-from . import formats, layout, quant, gemm  # noqa: F401
+from . import formats, layout, quant, gemm, moe  # noqa: F401
