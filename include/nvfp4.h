@@ -218,6 +218,84 @@ nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const in
                                   const float *alpha, void *d, int64_t t, int64_t n, int64_t k,
                                   uint32_t flags, nvfp4_stream_t stream);
 
+/* ---------------------------------------------------------------- MoE steps (NVFP4)
+ * The steps around the grouped GEMMs of an NVFP4 mixture-of-experts layer:
+ *   moe_sort_by_expert -> moe_gather_rows -> nvfp4_quantize_experts -> nvfp4_grouped_gemm (gate+up)
+ *   -> nvfp4_silu_mul_quantize_experts -> nvfp4_grouped_gemm (down) -> moe_combine.
+ * [vLLM-SM103] ops.h / torch_bindings.cpp name scaled_fp4_experts_quant,
+ * silu_and_mul_scaled_fp4_experts_quant (arguments input_offset_by_experts,
+ * output_scale_offset_by_experts) and cutlass_fp4_group_mm; [vLLM-51158] "Changes" describes the
+ * experts-quantise + grouped-GEMM structure.  The pages give names and arguments only; the
+ * definitions below are this library's reading of them. */
+
+/* Stable sort of routed (token, slot) pairs by expert.
+ *   topk_ids     DEVICE int32 [num_tokens, topk], expert of each slot (0 <= id < num_experts;
+ *                other values are dropped (pos = -1) and make nvfp4_check_status report
+ *                NVFP4_ERR_INVALID_ARG)
+ *   row_offsets  DEVICE int64 [num_experts + 1] out: rows of expert e are row_offsets[e] ..
+ *                row_offsets[e+1]-1 of the permuted order (the grouped kernels' row_offsets)
+ *   src_rows     DEVICE int32 [num_tokens * topk] out: token of each permuted row
+ *   pos          DEVICE int32 [num_tokens, topk] out: permuted row of each (token, slot)
+ * Inside an expert, rows keep (token, slot) row-major order.  1 <= topk <= 32,
+ * 1 <= num_experts <= 1024.  One CTA; cost grows with num_tokens / 32 per warp. */
+nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
+                                  int64_t *row_offsets, int32_t *src_rows, int32_t *pos, uint32_t flags,
+                                  nvfp4_stream_t stream);
+
+/* Row gather (permutation into expert order): out[r, :] = x[src_rows[r], :] for r < rows.
+ *   x        bf16 [num_tokens, h], row stride ldx (ldx >= h, ldx % 8 == 0), 16-B aligned
+ *   out      bf16 [rows, h] contiguous, 16-B aligned; h % 8 == 0
+ * A src_rows entry outside [0, num_tokens) is skipped (that row is not written) and makes
+ * nvfp4_check_status report NVFP4_ERR_INVALID_ARG. */
+nvfp4_status_t moe_gather_rows(const void *x, int64_t num_tokens, int64_t h, int64_t ldx, const int32_t *src_rows,
+                               int64_t rows, void *out, uint32_t flags, nvfp4_stream_t stream);
+
+/* Per-expert NVFP4 quantisation (scaled_fp4_experts_quant): rows of expert e (row_offsets as
+ * moe_sort_by_expert writes them) are quantised as nvfp4_quantize does with global scale gs[e];
+ * expert e's scales form their own zero-padded 128-row block starting at scale row
+ * sum_{j<e} round_up(M_j, 128) of a round_up(k/16, 4)-column 128x4-swizzled matrix.
+ *   x      bf16 [t, k], row stride ldx, 16-B aligned;  gs  DEVICE fp32 [num_experts]
+ *   q      uint8 [t, k/2], 8-B aligned
+ *   sf     uint8 [sf_bytes], 16-B aligned, sf_bytes >= (round_up(t,128) + 128*num_experts) *
+ *          round_up(k/16, 4)  (the same bound as mxfp4_grouped_sf_bytes with k/16 columns)
+ *   k % 16 == 0, 1 <= num_experts <= 1024. */
+nvfp4_status_t nvfp4_quantize_experts(const void *x, int64_t t, int64_t k, int64_t ldx, const int64_t *row_offsets,
+                                      int num_experts, const float *gs, uint8_t *q, uint8_t *sf, size_t sf_bytes,
+                                      uint32_t flags, nvfp4_stream_t stream);
+
+/* SiLU-and-mul fused with the per-expert NVFP4 quantisation (silu_and_mul_scaled_fp4_experts_quant).
+ * x is bf16 [t, 2*inter] = [gate | up]; the quantised matrix is h [t, inter] with
+ *   h = bf16(silu(gate) * up),  silu(g) = g * (1 / (1 + exp(-g)))  in fp32,
+ * exp computed by Cody-Waite range reduction and a degree-7 Taylor polynomial, every fp32 step
+ * rounded to nearest even (so the result equals "silu_and_mul to bf16, then quantise" done the
+ * same way), then h is quantised as nvfp4_quantize_experts does (q [t, inter/2], sf as there
+ * with k = inter).  ldx >= 2*inter, inter % 16 == 0. */
+nvfp4_status_t nvfp4_silu_mul_quantize_experts(const void *x, int64_t t, int64_t inter, int64_t ldx,
+                                               const int64_t *row_offsets, int num_experts, const float *gs,
+                                               uint8_t *q, uint8_t *sf, size_t sf_bytes, uint32_t flags,
+                                               nvfp4_stream_t stream);
+
+/* NVFP4 grouped (MoE) GEMM (cutlass_fp4_group_mm): D[rows of e, :] = alpha[e] * deq(A_e) deq(B_e)^T.
+ *   a      uint8 [t, k/2] rows sorted by expert;  sfa  as nvfp4_quantize_experts writes it
+ *   b      uint8 [num_experts, n, k/2];  sfb  uint8 [num_experts, nvfp4_sf_bytes(n, k, 16)]
+ *   alpha  DEVICE fp32 [num_experts] (one per expert: 1/(gsA_e * gsB_e)) or NULL for 1.0
+ *   d      bf16 [t, n], 32-B aligned;  n % 32 == 0, k % 32 == 0.
+ * Same kernel, checks and PDL behaviour as mxfp4_grouped_gemm. */
+nvfp4_status_t nvfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const int64_t *row_offsets, int num_experts,
+                                  const uint8_t *b, const uint8_t *sfb, const float *alpha, void *d, int64_t t,
+                                  int64_t n, int64_t k, uint32_t flags, nvfp4_stream_t stream);
+
+/* Weighted combine of the experts' outputs:
+ *   out[t, :] = bf16( sum_{j < topk} weights[t, j] * y[pos[t, j], :] )
+ * in fp32, slots in order, each product and sum rounded (no fused multiply-add); slots with
+ * pos < 0 are skipped (a token with none gets zeros); pos >= rows is skipped too and makes
+ * nvfp4_check_status report NVFP4_ERR_INVALID_ARG.
+ *   y        bf16 [rows, h] (expert order), 16-B aligned;  pos  DEVICE int32 [num_tokens, topk]
+ *   weights  DEVICE fp32 [num_tokens, topk];  out  bf16 [num_tokens, h], 16-B aligned;  h % 8 == 0 */
+nvfp4_status_t moe_combine(const void *y, int64_t rows, const int32_t *pos, const float *weights,
+                           int64_t num_tokens, int topk, int64_t h, void *out, uint32_t flags,
+                           nvfp4_stream_t stream);
+
 /* Scale layout conversion between a row-major scale matrix [rows, cols] (bytes) and the
  * 128x4 swizzled layout of nvfp4_sf_bytes size (swizzle writes the zero padding).
  * Source: [vLLM-SM103] nvfp4_utils.py swizzle_blockscale (pad to (128,4), then block
@@ -242,8 +320,8 @@ nvfp4_status_t nvfp4_sf_convert_layout(const uint8_t *src, uint8_t *dst, int64_t
                                        int to_sm103, nvfp4_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device status word that kernels set when a
- * bounded pipeline wait gave up or a grouped GEMM found malformed row offsets.  Returns
- * NVFP4_ERR_INVALID_ARG for malformed offsets (the kernel did no work), NVFP4_ERR_TIMEOUT if a
+ * bounded pipeline wait gave up, a grouped GEMM found malformed row offsets or a MoE step found
+ * an index out of range.  Returns NVFP4_ERR_INVALID_ARG for malformed offsets or indices, NVFP4_ERR_TIMEOUT if a
  * kernel timed out since the last check, NVFP4_ERR_CUDA if the synchronisation failed,
  * NVFP4_OK otherwise. */
 nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream);

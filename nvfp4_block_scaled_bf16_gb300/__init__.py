@@ -48,6 +48,12 @@ _SIGS = {
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_sf_convert_layout": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
+    "moe_sort_by_expert": (_int, [_vp, _i64, _int, _int, _vp, _vp, _vp, _u32, _vp]),
+    "moe_gather_rows": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
+    "nvfp4_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
+    "nvfp4_silu_mul_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
+    "nvfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
+    "moe_combine": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _i64, _vp, _u32, _vp]),
     "nvfp4_check_status": (_int, [_vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -260,6 +266,104 @@ def sf_convert_layout(src, rows: int, cols: int, to_sm103: bool = True, dst=None
         dst = torch.empty_like(src)
     _check(_lib.nvfp4_sf_convert_layout(_ptr(src), _ptr(dst), rows, cols, 1 if to_sm103 else 0, _stream(stream)))
     return dst
+
+
+# ---------------------------------------------------------------- MoE steps (NVFP4)
+def expert_sf_bytes(total_rows: int, experts: int, k: int) -> int:
+    """Grouped NVFP4 scale buffer bound: (round_up(t,128) + 128 E) * round_up(k/16, 4)."""
+    return (-(-total_rows // 128) * 128 + 128 * experts) * (-(-(k // 16) // 4) * 4)
+
+
+def moe_sort_by_expert(topk_ids, num_experts: int, flags: int = 0, stream=None):
+    """int32 [T, topk] expert ids -> (row_offsets int64 [E+1], src_rows int32 [T*topk],
+    pos int32 [T, topk]); stable: (token, slot) order inside an expert."""
+    _need(topk_ids, torch.int32, "topk_ids", 2)
+    topk_ids = topk_ids.contiguous()
+    T, topk = topk_ids.shape
+    dv = topk_ids.device
+    ro = torch.empty(num_experts + 1, dtype=torch.int64, device=dv)
+    src = torch.empty(T * topk, dtype=torch.int32, device=dv)
+    pos = torch.empty((T, topk), dtype=torch.int32, device=dv)
+    _check(_lib.moe_sort_by_expert(_ptr(topk_ids), T, topk, num_experts, _ptr(ro), _ptr(src), _ptr(pos), flags,
+                                   _stream(stream)))
+    return ro, src, pos
+
+
+def moe_gather_rows(x, src_rows, out=None, flags: int = 0, stream=None):
+    """out[r] = x[src_rows[r]] (bf16 rows)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(src_rows, torch.int32, "src_rows", 1)
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    T, h = x.shape
+    rows = src_rows.numel()
+    if out is None:
+        out = torch.empty((rows, h), dtype=torch.bfloat16, device=x.device)
+    _check(_lib.moe_gather_rows(_ptr(x), T, h, x.stride(0), _ptr(src_rows), rows, _ptr(out), flags, _stream(stream)))
+    return out
+
+
+def nvfp4_quantize_experts(x, row_offsets, gs, q=None, sf=None, flags: int = 0, stream=None):
+    """bf16 [t, k] (rows by expert) -> (packed e2m1 [t, k/2], grouped e4m3 scales); gs fp32 [E]."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(row_offsets, torch.int64, "row_offsets", 1)
+    _need(gs, torch.float32, "gs", 1)
+    t, k = x.shape
+    experts = row_offsets.numel() - 1
+    if q is None:
+        q = torch.empty((t, k // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(expert_sf_bytes(t, experts, k), dtype=torch.uint8, device=x.device)
+    _check(_lib.nvfp4_quantize_experts(_ptr(x), t, k, x.stride(0), _ptr(row_offsets), experts, _ptr(gs), _ptr(q),
+                                       _ptr(sf), sf.numel(), flags, _stream(stream)))
+    return q, sf
+
+
+def nvfp4_silu_mul_quantize_experts(x, row_offsets, gs, q=None, sf=None, flags: int = 0, stream=None):
+    """bf16 [t, 2I] = [gate | up] -> NVFP4 of h = bf16(silu(gate) * up): (q [t, I/2], grouped scales)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(row_offsets, torch.int64, "row_offsets", 1)
+    _need(gs, torch.float32, "gs", 1)
+    t, w = x.shape
+    inter = w // 2
+    experts = row_offsets.numel() - 1
+    if q is None:
+        q = torch.empty((t, inter // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(expert_sf_bytes(t, experts, inter), dtype=torch.uint8, device=x.device)
+    _check(_lib.nvfp4_silu_mul_quantize_experts(_ptr(x), t, inter, x.stride(0), _ptr(row_offsets), experts, _ptr(gs),
+                                                _ptr(q), _ptr(sf), sf.numel(), flags, _stream(stream)))
+    return q, sf
+
+
+def nvfp4_grouped_gemm(a, sfa, row_offsets, b, sfb, alpha=None, d=None, flags: int = 0, stream=None):
+    """Per expert e: D[rows of e] = bf16(alpha[e] * deq(A_e) @ deq(B_e)^T); b [E, n, k/2], alpha fp32 [E]."""
+    _need(a, torch.uint8, "a", 2)
+    _need(b, torch.uint8, "b", 3)
+    _need(row_offsets, torch.int64, "row_offsets", 1)
+    t, kh = a.shape
+    experts, n, kb = b.shape
+    if kb != kh or row_offsets.numel() != experts + 1 or (alpha is not None and alpha.numel() != experts):
+        raise ValueError("shape mismatch")
+    if d is None:
+        d = torch.empty((t, n), dtype=torch.bfloat16, device=a.device)
+    _check(_lib.nvfp4_grouped_gemm(_ptr(a), _ptr(sfa), _ptr(row_offsets), experts, _ptr(b), _ptr(sfb), _ptr(alpha),
+                                   _ptr(d), t, n, 2 * kh, flags, _stream(stream)))
+    return d
+
+
+def moe_combine(y, pos, weights, out=None, flags: int = 0, stream=None):
+    """out[t] = bf16(sum_j weights[t, j] * y[pos[t, j]]) (fp32, slot order)."""
+    _need(y, torch.bfloat16, "y", 2)
+    _need(pos, torch.int32, "pos", 2)
+    _need(weights, torch.float32, "weights", 2)
+    rows, h = y.shape
+    T, topk = pos.shape
+    if out is None:
+        out = torch.empty((T, h), dtype=torch.bfloat16, device=y.device)
+    _check(_lib.moe_combine(_ptr(y), rows, _ptr(pos.contiguous()), _ptr(weights.contiguous()), T, topk, h, _ptr(out),
+                            flags, _stream(stream)))
+    return out
 
 
 def check_status(stream=None) -> None:

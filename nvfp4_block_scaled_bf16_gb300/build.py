@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libnvfp4.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]
-SOURCES = ["api.cu", "quant.cu", "swizzle.cu", "gemm.cu", "grouped.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "swizzle.cu", "gemm.cu", "grouped.cu", "noalloc.cu", "moe.cu"]
 
 
 def nvcc() -> str:

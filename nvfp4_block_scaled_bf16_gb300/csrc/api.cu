@@ -199,6 +199,8 @@ extern "C" nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream) {
     cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (word & 2u)
       return fail(NVFP4_ERR_INVALID_ARG, "a grouped kernel found malformed row offsets and did no work (status 0x%x)", word);
+    if (word & 8u)
+      return fail(NVFP4_ERR_INVALID_ARG, "a MoE step found an expert id or row index out of range and skipped it (status 0x%x)", word);
     if (word & 4u)
       return fail(NVFP4_ERR_CUDA, "internal: a split tile had more partials than the fix-up buffer holds (status 0x%x)", word);
     static const char *const kSites[7] = {"load/free-slot", "mma/accumulator", "mma/stage", "mma/scales",

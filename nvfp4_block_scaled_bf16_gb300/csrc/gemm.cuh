@@ -150,6 +150,7 @@ struct GemmArgs {
   int lookahead;              // > 0: at most this many K stages in flight per CTA (stage i + L is
                               // issued once stage i has landed); 0: as many as the ring holds
   int sf_sm103;               // 1: both scale buffers are in the SM103 layout
+  int alpha_per_expert;       // grouped: alpha points to one fp32 per expert
 };
 
 // The 16 scale bytes of 512-byte scale tile `tile` that lane i of a scale writer puts in its
@@ -173,6 +174,7 @@ struct TileInfo {
   int sfb_blocks;              // B scale blocks present (<= SFB_BLOCKS)
   int rows, cols;              // valid rows of A / of B in this tile
   int64_t out_i0, out_j0;      // output coordinates of C[0][0] of the tile (before swap)
+  int expert;                  // grouped: the tile's expert
 };
 
 // One piece of a CTA's work: K stages [kt0, kt1) of tile `tile`.  n CTAs share the tile (n == 1:
@@ -264,6 +266,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C,
       else hi = mid - 1;
     }
     const int e = lo;
+    t.expert = e;
     const int rows_e = tb.ro[e + 1] - tb.ro[e];
     const int mt_e = (rows_e + 127) / 128;
     const int local = tile - tb.tp[e];
@@ -288,6 +291,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C,
     t.cols = min(C::BN, p.n - t.b_y);
     t.out_i0 = t.a_y;
     t.out_j0 = t.b_y;
+    t.expert = 0;
   }
   t.sfb_blocks = min(C::SFB_BLOCKS, (t.cols + 127) / 128);
   return t;
@@ -832,6 +836,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
       const bool ok = mbar_wait(smem_u32(&accf[acc]), acc_phase, wc, kSiteEpilogue);
       tc_fence_after();
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
+      const float tile_alpha = (GROUPED && p.alpha_per_expert && p.alpha) ? __ldg(p.alpha + t.expert) : alpha;
       float *red = reinterpret_cast<float *>(smem);
       float *slot = sk_part ? sk_slot<C>(p, blockIdx.x, sg.j) : nullptr;
 #pragma unroll 1
@@ -859,8 +864,8 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
               uint32_t v[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                v[i] = pack_bf16x2(__fmul_rn(alpha, __uint_as_float(r[16 * h + 2 * i])),
-                                   __fmul_rn(alpha, __uint_as_float(r[16 * h + 2 * i + 1])));
+                v[i] = pack_bf16x2(__fmul_rn(tile_alpha, __uint_as_float(r[16 * h + 2 * i])),
+                                   __fmul_rn(tile_alpha, __uint_as_float(r[16 * h + 2 * i + 1])));
               st_global_v8(out + 16 * h, v);
             }
           }

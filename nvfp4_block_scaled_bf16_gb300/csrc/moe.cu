@@ -1,0 +1,411 @@
+// The MoE steps around the grouped GEMMs, NVFP4 flavour: expert sort of the routed tokens,
+// row gather, per-expert NVFP4 quantisation (plain, or fused with SiLU-and-mul), weighted
+// combine.  Named on vLLM fork compare view "add pdl" (ops.h, torch_bindings.cpp:
+// scaled_fp4_experts_quant, silu_and_mul_scaled_fp4_experts_quant with input_offset_by_experts /
+// output_scale_offset_by_experts) and vLLM PR 51158 "Changes" (experts quantise, grouped GEMM);
+// the pages give names and arguments only, the definitions used are stated per entry point in
+// nvfp4.h.  All of these are bandwidth-bound CUDA-core kernels.
+#include <cuda_bf16.h>
+
+#include "host.h"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+namespace {
+
+constexpr int kMaxExpertsMoe = 1024;
+
+// ------------------------------------------------------------------ expert sort
+// One CTA of 1024 threads (32 warps).  Warp w owns tokens [w*tpw, (w+1)*tpw).
+//   1. per-warp expert counts (shared-memory atomics: order does not matter for counts);
+//   2. thread v turns the counts of expert v into per-warp starting rows, and a block scan over
+//      experts gives row_offsets;
+//   3. every warp walks its tokens in order, lanes = slots of one token; lanes holding the same
+//      expert (a repeated id) are ranked by slot with __match_any_sync, so the order inside an
+//      expert is (token, slot) order: a stable sort.
+// Ids outside [0, E) set bit 3 of the status word; such entries are dropped (no row, pos = -1).
+constexpr int kSortWarps = 32;
+
+__global__ void __launch_bounds__(kSortWarps * 32) moe_sort_kernel(const int32_t *__restrict__ ids, int T, int topk,
+                                                                   int E, int64_t *__restrict__ row_offsets,
+                                                                   int32_t *__restrict__ src, int32_t *__restrict__ pos,
+                                                                   unsigned int *status) {
+  extern __shared__ int32_t cnt[];  // [kSortWarps][E]
+  __shared__ int32_t tot[kMaxExpertsMoe + 1];
+  pdl_wait();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int i = threadIdx.x; i < kSortWarps * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int tpw = (T + kSortWarps - 1) / kSortWarps;
+  const int t0 = warp * tpw, t1 = min(T, t0 + tpw);
+  for (int e = t0 * topk + lane; e < t1 * topk; e += 32) {
+    const int v = ids[e];
+    if (v >= 0 && v < E) atomicAdd(&cnt[warp * E + v], 1);
+    else atomicOr(status, 8u);
+  }
+  __syncthreads();
+  // per-warp exclusive offsets inside each expert, expert totals
+  for (int v = threadIdx.x; v < E; v += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kSortWarps; ++w) {
+      const int c = cnt[w * E + v];
+      cnt[w * E + v] = run;
+      run += c;
+    }
+    tot[v] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {  // E <= 1024 sequential adds: negligible next to the rest
+    int64_t acc = 0;
+    for (int v = 0; v < E; ++v) {
+      const int c = tot[v];
+      tot[v] = static_cast<int>(acc);
+      row_offsets[v] = acc;
+      acc += c;
+    }
+    row_offsets[E] = acc;
+  }
+  __syncthreads();
+  for (int t = t0; t < t1; ++t) {
+    const bool active = lane < topk;
+    const int v = active ? ids[t * topk + lane] : -1;
+    const bool ok = active && v >= 0 && v < E;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? v : -1 - lane);  // invalid lanes alone
+    const int rank = __popc(peers & ((1u << lane) - 1));
+    int base = 0;
+    if (ok && rank == 0) {  // the lowest lane of each group bumps the counter for the group
+      base = cnt[warp * E + v];
+      cnt[warp * E + v] = base + __popc(peers);
+    }
+    base = __shfl_sync(0xFFFFFFFFu, base, __ffs(peers) - 1);
+    if (active) {
+      if (ok) {
+        const int row = tot[v] + base + rank;
+        src[row] = t;
+        pos[t * topk + lane] = row;
+      } else {
+        pos[t * topk + lane] = -1;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------ row gather
+// out[r, :] = x[src[r], :] for r < rows; 16-byte pieces, grid-stride.  A source row outside
+// [0, T) sets bit 3 of the status word and its output row is left untouched.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict__ x, int64_t ldx16, int64_t T,
+                                                         const int32_t *__restrict__ src, int64_t rows,
+                                                         int64_t pieces, uint4 *__restrict__ out,
+                                                         unsigned int *status) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t total = rows * pieces;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t r = i / pieces, c = i - r * pieces;
+    const int64_t s = src[r];
+    if (s < 0 || s >= T) {
+      if (c == 0) atomicOr(status, 8u);
+      continue;
+    }
+    out[r * pieces + c] = __ldg(x + s * ldx16 + c);
+  }
+}
+
+// ------------------------------------------------------------------ weighted combine
+// out[t, :] = bf16(sum_j w[t, j] * y[pos[t, j], :]), fp32 products and sums in slot order, no
+// fused multiply-add; a slot with pos < 0 (an entry the sort dropped) contributes nothing.
+// One thread per 8 output elements (16-byte loads of y, 16-byte store).
+__global__ void __launch_bounds__(256) moe_combine_kernel(const uint4 *__restrict__ y, int64_t rows,
+                                                          const int32_t *__restrict__ pos,
+                                                          const float *__restrict__ w, int64_t T, int topk,
+                                                          int64_t pieces, uint4 *__restrict__ out,
+                                                          unsigned int *status) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t total = T * pieces;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t t = i / pieces, c = i - t * pieces;
+    float acc[8];
+    bool first = true;
+    for (int j = 0; j < topk; ++j) {
+      const int64_t p = pos[t * topk + j];
+      if (p < 0) continue;
+      if (p >= rows) {
+        if (c == 0) atomicOr(status, 8u);
+        continue;
+      }
+      const float wj = w[t * topk + j];
+      const uint4 v = __ldg(y + p * pieces + c);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = __uint_as_float(u[q] << 16), hi = __uint_as_float(u[q] & 0xFFFF0000u);
+        const float plo = __fmul_rn(wj, lo), phi = __fmul_rn(wj, hi);
+        acc[2 * q] = first ? plo : __fadd_rn(acc[2 * q], plo);
+        acc[2 * q + 1] = first ? phi : __fadd_rn(acc[2 * q + 1], phi);
+      }
+      first = false;
+    }
+    uint4 o;
+    uint32_t *op = &o.x;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) op[q] = first ? 0u : pack_bf16x2(acc[2 * q], acc[2 * q + 1]);
+    out[t * pieces + c] = o;
+  }
+}
+
+// ------------------------------------------------------------------ per-expert NVFP4 quantiser
+// exp(t) in fp32 by Cody and Waite's range reduction and a degree-7 Taylor polynomial, every
+// step rounded to nearest even and nothing fused (so it is reproducible off the GPU):
+//   n = rint(t * log2 e); r = (t - n*LN2_HI) - n*LN2_LO; p = Horner(1/k!, k = 7..0); exp = p*2^n
+// with LN2_HI = 0.693145751953125 (16 significant bits, so n*LN2_HI is exact), t > 88 -> inf,
+// t < -87 -> 0.  Within 1.2 fp32 ulps of exp on [-87, 88].
+__device__ __forceinline__ float exp_cw(float t) {
+  if (t > 88.0f) return __int_as_float(0x7F800000);
+  if (t < -87.0f) return 0.0f;
+  const float n = __int2float_rn(__float2int_rn(__fmul_rn(t, 1.44269502162933349609375f)));
+  const float r = __fsub_rn(__fsub_rn(t, __fmul_rn(n, 0.693145751953125f)), __fmul_rn(n, 1.428606765330187045037746429443359375e-06f));
+  float p = 1.98412701138295233249664306640625e-04f;  // 1/7!
+  p = __fadd_rn(__fmul_rn(r, p), 1.388888922519981861114501953125e-03f);  // 1/6!
+  p = __fadd_rn(__fmul_rn(r, p), 8.333333767950534820556640625e-03f);      // 1/5!
+  p = __fadd_rn(__fmul_rn(r, p), 4.16666679084300994873046875e-02f);       // 1/4!
+  p = __fadd_rn(__fmul_rn(r, p), 0.16666667163372039794921875f);          // 1/3!
+  p = __fadd_rn(__fmul_rn(r, p), 0.5f);
+  p = __fadd_rn(__fmul_rn(r, p), 1.0f);
+  p = __fadd_rn(__fmul_rn(r, p), 1.0f);
+  return __fmul_rn(p, __int_as_float((__float2int_rn(n) + 127) << 23));
+}
+
+// h = bf16(silu(g) * u), silu(g) = g * (1 / (1 + exp(-g))), returned as the fp32 value of h.
+__device__ __forceinline__ float silu_mul_bf16(float g, float u) {
+  const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_cw(-g)));
+  return __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(g, sig), u)));
+}
+
+__device__ __forceinline__ void bf16x8_to_f32_moe(const uint4 &v, float *f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ int64_t sf_off_128x4(int64_t r, int64_t j, int64_t cp) {
+  return ((r >> 7) * (cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+// One thread per (scale row, scale column) of the grouped padded scale matrix: expert e owns
+// scale rows sfr[e] .. sfr[e+1]-1 (sfr[e+1] - sfr[e] = round_up(M_e, 128)); rows past an
+// expert's last token and columns past K/16 get scale 0x00.  SILU: the 16 quantised values are
+// h = bf16(silu(x[r, c]) * x[r, I + c]) for the block's columns c (x is [T, 2I]).
+template <bool SILU>
+__global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *__restrict__ x, int64_t t,
+                                                           int64_t kb, int64_t ldx, int64_t up_off,
+                                                           const int64_t *__restrict__ row_offsets, int experts,
+                                                           const float *__restrict__ gs_e, uint8_t *__restrict__ q,
+                                                           uint8_t *__restrict__ sf, int64_t cap_rows, int64_t cp) {
+  __shared__ int64_t s_ro[kMaxExpertsMoe + 1];
+  __shared__ int64_t s_sfr[kMaxExpertsMoe + 1];
+  pdl_trigger();
+  pdl_wait();
+  for (int e = threadIdx.x; e <= experts; e += blockDim.x) s_ro[e] = row_offsets[e];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int64_t acc = 0;
+    s_sfr[0] = 0;
+    for (int e = 0; e < experts; ++e) {
+      int64_t cnt = s_ro[e + 1] - s_ro[e];
+      cnt = cnt < 0 ? 0 : cnt;
+      acc += (cnt + 127) / 128 * 128;
+      s_sfr[e + 1] = acc;
+    }
+  }
+  __syncthreads();
+  const int64_t rows = s_sfr[experts] < cap_rows ? s_sfr[experts] : cap_rows;
+  const int64_t total = rows * cp;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t s = idx / cp;
+    const int64_t j = idx - s * cp;
+    int lo = 0, hi = experts - 1;  // expert owning scale row s: largest e with s_sfr[e] <= s
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_sfr[mid] <= s) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t local = s - s_sfr[lo];
+    const int64_t r = s_ro[lo] + local;
+    uint32_t code = 0;
+    if (local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t && j < kb) {
+      const float gs = __ldg(gs_e + lo);
+      float f[16];
+      const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
+      bf16x8_to_f32_moe(__ldg(src), f);
+      bf16x8_to_f32_moe(__ldg(src + 1), f + 8);
+      if (SILU) {
+        float u[16];
+        const uint4 *up = reinterpret_cast<const uint4 *>(x + r * ldx + up_off + j * 16);
+        bf16x8_to_f32_moe(__ldg(up), u);
+        bf16x8_to_f32_moe(__ldg(up + 1), u + 8);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+      }
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
+      code = e4m3_code(sc);
+      const float sd = e4m3_value(code);
+      const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
+      float y0[8], y1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        y0[i] = __fmul_rn(f[i], inv);
+        y1[i] = __fmul_rn(f[8 + i], inv);
+      }
+      uint2 out;
+      out.x = e2m1x8(y0);
+      out.y = e2m1x8(y1);
+      *reinterpret_cast<uint2 *>(q + r * (kb * 8) + j * 8) = out;
+    }
+    // 4 lanes (scale columns 4c .. 4c+3, adjacent positions of one row) -> one 32-bit word
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+    if ((j & 3) == 0) *reinterpret_cast<uint32_t *>(sf + sf_off_128x4(s, j, cp)) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+}
+
+int moe_grid(int64_t threads, int sm_count) {
+  const int64_t blocks = ceil_div(threads, 256);
+  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
+                                             int64_t *row_offsets, int32_t *src_rows, int32_t *pos, uint32_t flags,
+                                             nvfp4_stream_t stream) {
+  clear_error();
+  if (num_tokens < 0 || topk < 1 || topk > 32 || num_experts < 1 || num_experts > kMaxExpertsMoe ||
+      num_tokens * topk >= (1LL << 31))
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: tokens=%lld topk=%d experts=%d (topk 1..32, experts 1..%d)",
+                (long long)num_tokens, topk, num_experts, kMaxExpertsMoe);
+  if (flags & ~(uint32_t)NVFP4_FLAG_PDL) return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: unknown flags 0x%x", flags);
+  if (!row_offsets || (num_tokens > 0 && (!topk_ids || !src_rows || !pos)))
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: null pointer");
+  if (!aligned(row_offsets, 8) || !aligned(topk_ids, 4) || !aligned(src_rows, 4) || !aligned(pos, 4))
+    return fail(NVFP4_ERR_MISALIGNED, "moe_sort_by_expert: row_offsets need 8-B, the int32 arrays 4-B alignment");
+  DeviceInfo dev;
+  nvfp4_status_t st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  const int smem = kSortWarps * num_experts * 4;
+  st = allow_smem(reinterpret_cast<const void *>(moe_sort_kernel), smem, dev.device);
+  if (st != NVFP4_OK) return st;
+  cudaError_t e = launch(moe_sort_kernel, dim3(1), dim3(kSortWarps * 32), smem, (cudaStream_t)stream,
+                         (flags & NVFP4_FLAG_PDL) != 0, 1, topk_ids, static_cast<int>(num_tokens), topk, num_experts,
+                         row_offsets, src_rows, pos, dev.status);
+  return check_launch(e, "moe_sort_by_expert");
+}
+
+extern "C" nvfp4_status_t moe_gather_rows(const void *x, int64_t num_tokens, int64_t h, int64_t ldx,
+                                          const int32_t *src_rows, int64_t rows, void *out, uint32_t flags,
+                                          nvfp4_stream_t stream) {
+  clear_error();
+  if (num_tokens < 0 || rows < 0 || h <= 0 || h % 8 || ldx < h || ldx % 8)
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_gather_rows: tokens=%lld rows=%lld h=%lld ldx=%lld (h, ldx multiples of 8)",
+                (long long)num_tokens, (long long)rows, (long long)h, (long long)ldx);
+  if (flags & ~(uint32_t)NVFP4_FLAG_PDL) return fail(NVFP4_ERR_INVALID_ARG, "moe_gather_rows: unknown flags 0x%x", flags);
+  if (rows == 0) return NVFP4_OK;
+  if (!x || !src_rows || !out) return fail(NVFP4_ERR_INVALID_ARG, "moe_gather_rows: null pointer");
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(src_rows, 4))
+    return fail(NVFP4_ERR_MISALIGNED, "moe_gather_rows: x and out need 16-B, src_rows 4-B alignment");
+  DeviceInfo dev;
+  nvfp4_status_t st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  const int64_t pieces = h / 8;
+  cudaError_t e = launch(moe_gather_kernel, dim3(moe_grid(rows * pieces, dev.sm_count)), dim3(256), 0,
+                         (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(x),
+                         ldx / 8, num_tokens, src_rows, rows, pieces, static_cast<uint4 *>(out), dev.status);
+  return check_launch(e, "moe_gather_rows");
+}
+
+extern "C" nvfp4_status_t moe_combine(const void *y, int64_t rows, const int32_t *pos, const float *weights,
+                                      int64_t num_tokens, int topk, int64_t h, void *out, uint32_t flags,
+                                      nvfp4_stream_t stream) {
+  clear_error();
+  if (num_tokens < 0 || rows < 0 || topk < 1 || h <= 0 || h % 8)
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_combine: tokens=%lld rows=%lld topk=%d h=%lld (h a multiple of 8)",
+                (long long)num_tokens, (long long)rows, topk, (long long)h);
+  if (flags & ~(uint32_t)NVFP4_FLAG_PDL) return fail(NVFP4_ERR_INVALID_ARG, "moe_combine: unknown flags 0x%x", flags);
+  if (num_tokens == 0) return NVFP4_OK;
+  if (!y || !pos || !weights || !out) return fail(NVFP4_ERR_INVALID_ARG, "moe_combine: null pointer");
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(pos, 4) || !aligned(weights, 4))
+    return fail(NVFP4_ERR_MISALIGNED, "moe_combine: y and out need 16-B, pos and weights 4-B alignment");
+  DeviceInfo dev;
+  nvfp4_status_t st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  const int64_t pieces = h / 8;
+  cudaError_t e = launch(moe_combine_kernel, dim3(moe_grid(num_tokens * pieces, dev.sm_count)), dim3(256), 0,
+                         (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(y), rows,
+                         pos, weights, num_tokens, topk, pieces, static_cast<uint4 *>(out), dev.status);
+  return check_launch(e, "moe_combine");
+}
+
+namespace {
+nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t t, int64_t k, int64_t ldx,
+                            const int64_t *row_offsets, int num_experts, const float *gs, uint8_t *q, uint8_t *sf,
+                            size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream) {
+  clear_error();
+  if (t < 0 || k <= 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: t=%lld k=%lld", name, (long long)t, (long long)k);
+  if (k % 16) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: k=%lld is not a multiple of 16", name, (long long)k);
+  const int64_t width = silu ? 2 * k : k;
+  if (ldx < width || ldx % 8)
+    return fail(NVFP4_ERR_MISALIGNED, "%s: ldx=%lld (need ldx >= %lld, ldx %% 8 == 0)", name, (long long)ldx, (long long)width);
+  if (num_experts < 1 || num_experts > kMaxExpertsMoe)
+    return fail(NVFP4_ERR_INVALID_ARG, "%s: num_experts=%d (1..%d)", name, num_experts, kMaxExpertsMoe);
+  if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT))
+    return fail(NVFP4_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
+  const int64_t cp = round_up(k / 16, 4);
+  const size_t need = static_cast<size_t>((round_up(t, 128) + 128LL * num_experts) * cp);
+  if (sf_bytes < need) return fail(NVFP4_ERR_INVALID_ARG, "%s: sf_bytes=%zu < %zu", name, sf_bytes, need);
+  if (t == 0) return NVFP4_OK;
+  if (!x || !row_offsets || !gs || !q || !sf) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (!aligned(x, 16) || !aligned(q, 8) || !aligned(sf, 16) || !aligned(row_offsets, 8) || !aligned(gs, 4))
+    return fail(NVFP4_ERR_MISALIGNED, "%s: x 16-B, q 8-B, sf 16-B, row_offsets 8-B, gs 4-B alignment", name);
+  DeviceInfo dev;
+  nvfp4_status_t st = current_device(&dev);
+  if (st != NVFP4_OK) return st;
+  const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
+  const int64_t total = (round_up(t, 128) + 128LL * num_experts) * cp;
+  auto kern = silu ? expert_quant_kernel<true> : expert_quant_kernel<false>;
+  cudaError_t e = launch(kern, dim3(moe_grid(total, dev.sm_count)), dim3(256), 0, (cudaStream_t)stream,
+                         (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x), t, k / 16, ldx,
+                         silu ? k : static_cast<int64_t>(0), row_offsets, num_experts, gs, q, sf, cap_rows, cp);
+  return check_launch(e, name);
+}
+}  // namespace
+
+extern "C" nvfp4_status_t nvfp4_quantize_experts(const void *x, int64_t t, int64_t k, int64_t ldx,
+                                                 const int64_t *row_offsets, int num_experts, const float *gs,
+                                                 uint8_t *q, uint8_t *sf, size_t sf_bytes, uint32_t flags,
+                                                 nvfp4_stream_t stream) {
+  return expert_quant("nvfp4_quantize_experts", false, x, t, k, ldx, row_offsets, num_experts, gs, q, sf, sf_bytes,
+                      flags, stream);
+}
+
+extern "C" nvfp4_status_t nvfp4_silu_mul_quantize_experts(const void *x, int64_t t, int64_t inter, int64_t ldx,
+                                                          const int64_t *row_offsets, int num_experts,
+                                                          const float *gs, uint8_t *q, uint8_t *sf, size_t sf_bytes,
+                                                          uint32_t flags, nvfp4_stream_t stream) {
+  return expert_quant("nvfp4_silu_mul_quantize_experts", true, x, t, inter, ldx, row_offsets, num_experts, gs, q, sf,
+                      sf_bytes, flags, stream);
+}

@@ -1,0 +1,187 @@
+"""GPU parity of the NVFP4 MoE steps against oracle/moe.py: the expert sort, gather and combine
+bit-exact, the per-expert quantisers (plain and SiLU-fused) bit-exact, the NVFP4 grouped GEMM
+within |D - R| <= ulp_bf16(|R|) + 1e-5 * sum_k |alpha a b|; and the whole layer chained, each
+step checked on the GPU's own input to it."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from cases import dev
+from oracle import gemm as ogemm
+from oracle import moe
+from oracle import quant as oquant
+
+pytestmark = pytest.mark.gpu
+F32 = np.float32
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_block_scaled_bf16_gb300 as m
+    return m
+
+
+def _route(T, E, topk, seed, dup=False):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn(T, E, generator=g)
+    w, ids = torch.topk(torch.softmax(logits, dim=1), topk, dim=1)
+    ids = ids.to(torch.int32)
+    if dup:   # repeated experts inside a token: the sort must still be stable
+        ids[::3, 1] = ids[::3, 0]
+    return ids, w.float()
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=F32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("T,E,topk,dup", [(1, 1, 1, False), (7, 4, 2, False), (300, 16, 8, False),
+                                          (4096, 128, 8, False), (1000, 32, 4, True), (33, 1024, 32, False)])
+def test_sort_gather_combine(nv, T, E, topk, dup):
+    ids, w = _route(T, E, topk, T + E, dup)
+    ro, src, pos = nv.moe_sort_by_expert(ids.cuda(), E)
+    torch.cuda.synchronize()
+    nv.check_status()
+    o_ro, o_src, o_pos = moe.sort_by_expert(ids.numpy(), E)
+    assert np.array_equal(ro.cpu().numpy(), o_ro)
+    assert np.array_equal(src.cpu().numpy(), o_src)
+    assert np.array_equal(pos.cpu().numpy(), o_pos)
+    H = 64
+    x = _bf16(np.random.default_rng(T).standard_normal((T, H)))
+    xg = nv.moe_gather_rows(x.cuda(), src)
+    torch.cuda.synchronize()
+    assert torch.equal(xg.cpu(), x[torch.from_numpy(o_src)])
+    y = _bf16(np.random.default_rng(T + 1).standard_normal((T * topk, H)))
+    out = nv.moe_combine(y.cuda(), pos, w.cuda())
+    torch.cuda.synchronize()
+    nv.check_status()
+    want = moe.combine(y.float().numpy(), o_pos, w.numpy())
+    assert np.array_equal(out.float().cpu().numpy(), want)
+
+
+def test_sort_rejects_bad_ids_on_the_device(nv):
+    ids = torch.tensor([[0, 5], [1, 2]], dtype=torch.int32, device="cuda")   # 5 >= E
+    ro, src, pos = nv.moe_sort_by_expert(ids, 4)
+    with pytest.raises(nv.NVFP4Error):
+        nv.check_status()
+    assert pos.cpu().tolist() == [[0, -1], [1, 2]] and ro.cpu().tolist() == [0, 1, 2, 3, 3]
+
+
+def _counts_to_offsets(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+
+
+@pytest.mark.parametrize("counts,k", [([5], 64), ([0, 3, 130, 0, 1, 64], 96), ([256] * 4, 2048),
+                                      (list(np.random.default_rng(0).integers(0, 300, 128)), 768)])
+def test_quantize_experts_bit_exact(nv, counts, k):
+    ro = _counts_to_offsets(counts)
+    T = int(ro[-1])
+    E = len(counts)
+    x = synth.activation(T + k, T, k, outliers=False)
+    gs = (np.random.default_rng(k).uniform(100, 3000, E)).astype(F32)
+    q, sf = nv.nvfp4_quantize_experts(x.cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(gs).cuda())
+    torch.cuda.synchronize()
+    oq, osf = moe.nvfp4_quantize_experts(x, ro, gs)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(sf.cpu().numpy()[:osf.size], osf)
+
+
+@pytest.mark.parametrize("counts,inter", [([4], 32), ([0, 7, 129, 1], 64), (list(np.random.default_rng(1).integers(0, 300, 128)), 768)])
+def test_silu_mul_quantize_experts_bit_exact(nv, counts, inter):
+    ro = _counts_to_offsets(counts)
+    T = int(ro[-1])
+    E = len(counts)
+    x = synth.activation(T + inter, T, 2 * inter, outliers=False)
+    # include large-magnitude gate values (exp overflow / underflow branches)
+    x[: min(T, 3), :4] = torch.tensor([90.0, -90.0, 0.0, -0.0], dtype=torch.bfloat16)
+    gs = (np.random.default_rng(inter).uniform(10, 3000, E)).astype(F32)
+    q, sf = nv.nvfp4_silu_mul_quantize_experts(x.cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(gs).cuda())
+    torch.cuda.synchronize()
+    h = moe.silu_and_mul(x)
+    oq, osf = moe.nvfp4_quantize_experts(h, ro, gs)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(sf.cpu().numpy()[:osf.size], osf)
+
+
+def _expert_weights(E, N, K, seed):
+    qb, sfb, gsb = [], [], []
+    for e in range(E):
+        w = synth.weight(seed * 1000 + e, N, K)
+        g = F32(2688.0) / F32(w.float().abs().max().item())
+        q_, s_ = oquant.nvfp4_quantize(w, g)
+        qb.append(q_), sfb.append(s_), gsb.append(g)
+    return np.stack(qb), np.stack(sfb), np.array(gsb, dtype=F32)
+
+
+@pytest.mark.parametrize("counts,N,K", [([3, 0, 40], 64, 128), ([0, 130, 1, 257], 256, 512),
+                                        (list(np.random.default_rng(2).integers(0, 300, 16)), 1536, 2048)])
+def test_nvfp4_grouped_gemm(nv, counts, N, K):
+    ro = _counts_to_offsets(counts)
+    T, E = int(ro[-1]), len(counts)
+    x = synth.activation(T + N, T, K, outliers=False)
+    gsa = np.random.default_rng(N).uniform(500, 3000, E).astype(F32)
+    qa, sfa = moe.nvfp4_quantize_experts(x, ro, gsa)
+    qb, sfb, gsb = _expert_weights(E, N, K, N + K)
+    alpha = (F32(1.0) / (gsa * gsb)).astype(F32)
+    d = nv.nvfp4_grouped_gemm(dev(qa), dev(sfa), torch.from_numpy(ro).cuda(), dev(qb), dev(sfb),
+                              torch.from_numpy(alpha).cuda())
+    torch.cuda.synchronize()
+    nv.check_status()
+    res = moe.nvfp4_grouped_gemm(qa, sfa, ro, qb, sfb, alpha, N, K)
+    dd = d.float().cpu().numpy().astype(np.float64)
+    for e, (Ae, Be, Re) in res.items():
+        r0, r1 = int(ro[e]), int(ro[e + 1])
+        if r1 == r0:
+            continue
+        tol = ogemm.tolerance(Re, np.float64(alpha[e]) * (np.abs(Ae) @ np.abs(Be).T))
+        err = np.abs(dd[r0:r1] - Re)
+        assert np.all(err <= tol), (e, float((err / np.maximum(tol, 1e-300)).max()))
+
+
+def test_moe_layer_chained(nv):
+    """sort -> gather -> quantise -> gate+up GEMM -> SiLU*mul+quantise -> down GEMM -> combine, on
+    the GPU with PDL; every step compared with the oracle on the GPU's own input to it."""
+    T, E, topk, H, I = 256, 16, 4, 256, 128
+    ids, w = _route(T, E, topk, 11)
+    x = synth.activation(5, T, H, outliers=False)
+    gs1 = np.full(E, 500.0, F32)
+    gs2 = np.full(E, 2000.0, F32)
+    qw1, sfw1, gw1 = _expert_weights(E, 2 * I, H, 1)
+    qw2, sfw2, gw2 = _expert_weights(E, H, I, 2)
+    a1 = (F32(1.0) / (gs1 * gw1)).astype(F32)
+    a2 = (F32(1.0) / (gs2 * gw2)).astype(F32)
+    P = nv.FLAG_PDL
+    ro, src, pos = nv.moe_sort_by_expert(ids.cuda(), E, flags=P)
+    xg = nv.moe_gather_rows(x.cuda(), src, flags=P)
+    q1, s1 = nv.nvfp4_quantize_experts(xg, ro, torch.from_numpy(gs1).cuda(), flags=P)
+    h1 = nv.nvfp4_grouped_gemm(q1, s1, ro, dev(qw1), dev(sfw1), torch.from_numpy(a1).cuda(), flags=P)
+    q2, s2 = nv.nvfp4_silu_mul_quantize_experts(h1, ro, torch.from_numpy(gs2).cuda(), flags=P)
+    y = nv.nvfp4_grouped_gemm(q2, s2, ro, dev(qw2), dev(sfw2), torch.from_numpy(a2).cuda(), flags=P)
+    out = nv.moe_combine(y, pos, w.cuda(), flags=P)
+    torch.cuda.synchronize()
+    nv.check_status()
+    o_ro, o_src, o_pos = moe.sort_by_expert(ids.numpy(), E)
+    assert np.array_equal(ro.cpu().numpy(), o_ro) and np.array_equal(pos.cpu().numpy(), o_pos)
+    assert torch.equal(xg.cpu(), x[torch.from_numpy(o_src)])
+    oq1, os1 = moe.nvfp4_quantize_experts(xg.cpu(), o_ro, gs1)
+    assert np.array_equal(q1.cpu().numpy(), oq1) and np.array_equal(s1.cpu().numpy()[:os1.size], os1)
+    for (qa, sa, qb, sb, al, N, K, d) in ((oq1, os1, qw1, sfw1, a1, 2 * I, H, h1),):
+        res = moe.nvfp4_grouped_gemm(qa, sa, o_ro, qb, sb, al, N, K)
+        dd = d.float().cpu().numpy().astype(np.float64)
+        for e, (Ae, Be, Re) in res.items():
+            r0, r1 = int(o_ro[e]), int(o_ro[e + 1])
+            tol = ogemm.tolerance(Re, np.float64(al[e]) * (np.abs(Ae) @ np.abs(Be).T))
+            assert np.all(np.abs(dd[r0:r1] - Re) <= tol)
+    oq2, os2 = moe.nvfp4_quantize_experts(moe.silu_and_mul(h1.cpu()), o_ro, gs2)
+    assert np.array_equal(q2.cpu().numpy(), oq2) and np.array_equal(s2.cpu().numpy()[:os2.size], os2)
+    res = moe.nvfp4_grouped_gemm(oq2, os2, o_ro, qw2, sfw2, a2, H, I)
+    dd = y.float().cpu().numpy().astype(np.float64)
+    for e, (Ae, Be, Re) in res.items():
+        r0, r1 = int(o_ro[e]), int(o_ro[e + 1])
+        tol = ogemm.tolerance(Re, np.float64(a2[e]) * (np.abs(Ae) @ np.abs(Be).T))
+        assert np.all(np.abs(dd[r0:r1] - Re) <= tol)
+    want = moe.combine(y.float().cpu().numpy(), o_pos, w.numpy())
+    assert np.array_equal(out.float().cpu().numpy(), want)
