@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the NVFP4 quantise -> GEMM hot path on one GB300 (or N replicas).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|e2e|moe|pipeline]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|e2e|moe|moe_nvfp4|pipeline]
     python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
 
 Workloads (synthetic, seeded; shapes and value distributions of the pages' benchmarks):
@@ -16,6 +16,9 @@ Workloads (synthetic, seeded; shapes and value distributions of the pages' bench
   moe                 MXFP4: 4096 tokens top-8 over 128 experts (32768 rows); quantise, then the
                       gate+up grouped GEMM (N=1536, K=2048) and the down grouped GEMM (N=2048,
                       K=768) on a second quantised activation.
+  moe_nvfp4           a whole NVFP4 MoE layer (same shape as moe): expert sort, gather,
+                      quantise, gate+up grouped GEMM, fused SiLU*mul + quantise, down grouped
+                      GEMM, weighted combine, chained with PDL.
   pipeline            4 back-to-back quant->GEMM layers (N=K=7168, own weight per layer) at
                       M in {1,16,64,256,1024,2048,4096}; the line adds each M's 4-layer time
                       with and without PDL.
@@ -272,6 +275,79 @@ def make_moe(nv):
     return wl
 
 
+def nvfp4_grouped_bytes(experts, t, n, k):
+    return experts * n * k * (1 / 2 + 1 / 16) + t * k * (1 / 2 + 1 / 16) + 2 * t * n
+
+
+def make_moe_nvfp4(nv):
+    """A whole NVFP4 MoE layer (the f3 steps): sort -> gather -> quantise -> gate+up grouped GEMM
+    -> SiLU*mul + quantise -> down grouped GEMM -> combine, chained with PDL.  128 experts, 4096
+    tokens top-8, hidden 2048, expert intermediate 768 (the MXFP4 MoE shape, NVFP4 formats)."""
+    wl = Workload(nv, "moe_nvfp4")
+    E, T, topk, H, I = 128, 4096, 8, 2048, 768
+    ids, wts = synth.moe_topk(0, T, E, topk)
+    x = synth.activation(20, T, H, outliers=False)
+    ids_d, wts_d, xd = ids.cuda(), wts.cuda(), x.cuda()
+    gs1 = torch.full((E,), _gs(x), dtype=torch.float32, device="cuda")
+    specs = {}
+    for name, n, k, seed in (("gate_up", 2 * I, H, 1), ("down", H, I, 2)):
+        qb = torch.empty((E, n, k // 2), dtype=torch.uint8, device="cuda")
+        sfb = torch.empty((E, nv.sf_bytes(n, k, 16)), dtype=torch.uint8, device="cuda")
+        gsb = torch.empty(E, dtype=torch.float32)
+        for e in range(E):
+            w = synth.weight(seed * 1000 + e, n, k)
+            gsb[e] = _gs(w)
+            nv.nvfp4_quantize(w.cuda(), gsb[e:e + 1].cuda(), q=qb[e], sf=sfb[e])
+        specs[name] = (qb, sfb, gsb)
+    R = T * topk
+    P = nv.FLAG_PDL
+    ro = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+    src = torch.empty(R, dtype=torch.int32, device="cuda")
+    pos = torch.empty((T, topk), dtype=torch.int32, device="cuda")
+    xg = torch.empty((R, H), dtype=torch.bfloat16, device="cuda")
+    q1 = torch.empty((R, H // 2), dtype=torch.uint8, device="cuda")
+    s1 = torch.empty(nv.expert_sf_bytes(R, E, H), dtype=torch.uint8, device="cuda")
+    h1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device="cuda")
+    q2 = torch.empty((R, I // 2), dtype=torch.uint8, device="cuda")
+    s2 = torch.empty(nv.expert_sf_bytes(R, E, I), dtype=torch.uint8, device="cuda")
+    y = torch.empty((R, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    a1 = (1.0 / (gs1.cpu() * specs["gate_up"][2])).to(torch.float32).cuda()
+    # the SiLU*mul output's global scale: calibrated once from a run of the first half
+    nv.moe_sort_by_expert(ids_d, E)
+    ro0, src0, _ = nv.moe_sort_by_expert(ids_d, E)
+    xq, xs = nv.nvfp4_quantize_experts(nv.moe_gather_rows(xd, src0), ro0, gs1)
+    hh = nv.nvfp4_grouped_gemm(xq, xs, ro0, specs["gate_up"][0], specs["gate_up"][1], a1)
+    hf = hh.float()
+    hamax = float((torch.nn.functional.silu(hf[:, :I]) * hf[:, I:]).abs().max().item())
+    gs2 = torch.full((E,), float(np.float32(2688.0) / np.float32(hamax)), dtype=torch.float32, device="cuda")
+    a2 = (1.0 / (gs2.cpu() * specs["down"][2])).to(torch.float32).cuda()
+    del xq, xs, hh, hf
+    L = wl.launches
+    sort_ws = torch.empty(max(1, nv.moe_sort_workspace_size(T, E) // 4), dtype=torch.int32, device="cuda")
+    L.append(lambda: nv.moe_sort_by_expert(ids_d, E, out=(ro, src, pos), workspace=sort_ws, flags=P))
+    L.append(lambda: nv.moe_gather_rows(xd, src, out=xg, flags=P))
+    L.append(lambda: nv.nvfp4_quantize_experts(xg, ro, gs1, q=q1, sf=s1, flags=P))
+    g1 = (lambda: nv.nvfp4_grouped_gemm(q1, s1, ro, specs["gate_up"][0], specs["gate_up"][1], a1, d=h1, flags=P))
+    L.append(g1)
+    L.append(lambda: nv.nvfp4_silu_mul_quantize_experts(h1, ro, gs2, q=q2, sf=s2, flags=P))
+    g2 = (lambda: nv.nvfp4_grouped_gemm(q2, s2, ro, specs["down"][0], specs["down"][1], a2, d=y, flags=P))
+    L.append(g2)
+    L.append(lambda: nv.moe_combine(y, pos, wts_d, out=out, flags=P))
+    wl.gemm_launches += [g1, g2]
+    wl.flops = 2.0 * R * (2 * I * H + H * I)
+    wl.gemm_bytes = nvfp4_grouped_bytes(E, R, 2 * I, H) + nvfp4_grouped_bytes(E, R, H, I)
+    wl.quant_bytes = quant_bytes(R, H) + quant_bytes(R, 2 * I)
+    wl.h2d += [(xd, x.pin_memory()), (ids_d, ids.pin_memory()), (wts_d, wts.pin_memory())]
+    wl.d2h.append((torch.empty((T, H), dtype=torch.bfloat16).pin_memory(), out))
+    wl.config = {"workload": "NVFP4 MoE layer: 128 experts, 4096 tokens top-8 (32768 rows), hidden 2048, intermediate "
+                             "768; sort, gather, quantise, gate+up grouped GEMM (N=1536, K=2048), SiLU*mul+quantise, "
+                             "down grouped GEMM (N=2048, K=768), combine",
+                 "global_batch": R, "inputs": "activation N(0,1), expert weights N(0,0.02), router logits N(0,1), seed 0",
+                 "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}
+    return wl
+
+
 PIPE_MS = (1, 16, 64, 256, 1024, 2048, 4096)
 PIPE_LAYERS = 4
 
@@ -304,7 +380,8 @@ def make_custom(nv, shapes):
     return wl
 
 
-MAKERS = {"decode": make_decode, "prefill": make_prefill, "e2e": make_e2e, "moe": make_moe, "pipeline": make_pipeline}
+MAKERS = {"decode": make_decode, "prefill": make_prefill, "e2e": make_e2e, "moe": make_moe, "pipeline": make_pipeline,
+          "moe_nvfp4": make_moe_nvfp4}
 
 
 # ---------------------------------------------------------------------------- timing
@@ -436,7 +513,7 @@ def run_ours(args, dist_on, rank, world):
     else:
         roof = {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak_tflops, 1),
                 "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak_tflops, 4), "traffic": None}
-    roof.update({"kernel": "bs_gemm_kernel" if wl.name != "moe" else "bs_gemm_kernel (grouped)",
+    roof.update({"kernel": "bs_gemm_kernel" if wl.name not in ("moe", "moe_nvfp4") else "bs_gemm_kernel (grouped)",
                  "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if bound == 'hbm' else 'bf16_tflops x 6, the nominal fp4/bf16 ratio'})",
                  "per_launch_ms": round(per_launch_ms, 5), "binding_roof_frac": round(t_roof / (gemm_mean * 1e-3), 4),
                  "bytes_per_step": wl.gemm_bytes})
@@ -499,9 +576,10 @@ def oracle_step(workload: str, n_rows_sample: int):
     dequantise, fp64 GEMM); returns (flops done, seconds, description)."""
     from oracle import gemm as ogemm
     from oracle import quant as oquant
-    if workload == "moe":
+    if workload in ("moe", "moe_nvfp4"):
         shapes = [(256, 1536, 2048), (256, 2048, 768)]     # one average expert, both GEMMs
-        desc = "one 256-row expert of each MoE GEMM (gate+up 1536x2048, down 2048x768), MXFP4"
+        fmt = "MXFP4" if workload == "moe" else "NVFP4"
+        desc = f"one 256-row expert of each MoE GEMM (gate+up 1536x2048, down 2048x768), {fmt}"
     elif workload == "prefill":
         shapes = [(64, n_rows_sample, k) for (_, n, k) in PREFILL]
         desc = f"64 activation rows x {n_rows_sample} weight rows of each prefill shape"
@@ -519,7 +597,7 @@ def oracle_step(workload: str, n_rows_sample: int):
     for i, (m, n, k) in enumerate(shapes):
         xa = synth.activation(i, m, k)
         xb = synth.weight(0, n, k)
-        if workload == "moe":
+        if workload == "moe":   # (moe_nvfp4 samples the NVFP4 path below)
             qa, sfa = oquant.mxfp4_quantize(xa)
             qb, sfb = oquant.mxfp4_quantize(xb)
             A = ogemm.dequantize(qa, sfa, m, k, 32, "ue8m0")

@@ -228,6 +228,9 @@ nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const in
  * experts-quantise + grouped-GEMM structure.  The pages give names and arguments only; the
  * definitions below are this library's reading of them. */
 
+/* Bytes of device workspace moe_sort_by_expert needs (one int32 count per CTA and expert).  Host only. */
+size_t moe_sort_workspace_size(int64_t num_tokens, int num_experts);
+
 /* Stable sort of routed (token, slot) pairs by expert.
  *   topk_ids     DEVICE int32 [num_tokens, topk], expert of each slot (0 <= id < num_experts;
  *                other values are dropped (pos = -1) and make nvfp4_check_status report
@@ -236,11 +239,13 @@ nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const in
  *                row_offsets[e+1]-1 of the permuted order (the grouped kernels' row_offsets)
  *   src_rows     DEVICE int32 [num_tokens * topk] out: token of each permuted row
  *   pos          DEVICE int32 [num_tokens, topk] out: permuted row of each (token, slot)
+ *   workspace    DEVICE, 4-B aligned, workspace_bytes >= moe_sort_workspace_size(); no
+ *                initialisation needed (every byte used is written first)
  * Inside an expert, rows keep (token, slot) row-major order.  1 <= topk <= 32,
- * 1 <= num_experts <= 1024.  One CTA; cost grows with num_tokens / 32 per warp. */
+ * 1 <= num_experts <= 1024.  Two kernels over ceil(num_tokens/32) CTAs (at most 1024). */
 nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
-                                  int64_t *row_offsets, int32_t *src_rows, int32_t *pos, uint32_t flags,
-                                  nvfp4_stream_t stream);
+                                  int64_t *row_offsets, int32_t *src_rows, int32_t *pos, int32_t *workspace,
+                                  size_t workspace_bytes, uint32_t flags, nvfp4_stream_t stream);
 
 /* Row gather (permutation into expert order): out[r, :] = x[src_rows[r], :] for r < rows.
  *   x        bf16 [num_tokens, h], row stride ldx (ldx >= h, ldx % 8 == 0), 16-B aligned

@@ -48,7 +48,8 @@ _SIGS = {
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_sf_convert_layout": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
-    "moe_sort_by_expert": (_int, [_vp, _i64, _int, _int, _vp, _vp, _vp, _u32, _vp]),
+    "moe_sort_workspace_size": (_sz, [_i64, _int]),
+    "moe_sort_by_expert": (_int, [_vp, _i64, _int, _int, _vp, _vp, _vp, _vp, _sz, _u32, _vp]),
     "moe_gather_rows": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
     "nvfp4_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
     "nvfp4_silu_mul_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
@@ -274,18 +275,27 @@ def expert_sf_bytes(total_rows: int, experts: int, k: int) -> int:
     return (-(-total_rows // 128) * 128 + 128 * experts) * (-(-(k // 16) // 4) * 4)
 
 
-def moe_sort_by_expert(topk_ids, num_experts: int, flags: int = 0, stream=None):
+def moe_sort_workspace_size(num_tokens: int, num_experts: int) -> int:
+    return int(_lib.moe_sort_workspace_size(num_tokens, num_experts))
+
+
+def moe_sort_by_expert(topk_ids, num_experts: int, out=None, workspace=None, flags: int = 0, stream=None):
     """int32 [T, topk] expert ids -> (row_offsets int64 [E+1], src_rows int32 [T*topk],
-    pos int32 [T, topk]); stable: (token, slot) order inside an expert."""
+    pos int32 [T, topk]); stable: (token, slot) order inside an expert.  `out` may pass the
+    three output tensors to fill."""
     _need(topk_ids, torch.int32, "topk_ids", 2)
     topk_ids = topk_ids.contiguous()
     T, topk = topk_ids.shape
     dv = topk_ids.device
-    ro = torch.empty(num_experts + 1, dtype=torch.int64, device=dv)
-    src = torch.empty(T * topk, dtype=torch.int32, device=dv)
-    pos = torch.empty((T, topk), dtype=torch.int32, device=dv)
-    _check(_lib.moe_sort_by_expert(_ptr(topk_ids), T, topk, num_experts, _ptr(ro), _ptr(src), _ptr(pos), flags,
-                                   _stream(stream)))
+    if out is None:
+        out = (torch.empty(num_experts + 1, dtype=torch.int64, device=dv),
+               torch.empty(T * topk, dtype=torch.int32, device=dv),
+               torch.empty((T, topk), dtype=torch.int32, device=dv))
+    ro, src, pos = out
+    if workspace is None:
+        workspace = torch.empty(max(1, moe_sort_workspace_size(T, num_experts) // 4), dtype=torch.int32, device=dv)
+    _check(_lib.moe_sort_by_expert(_ptr(topk_ids), T, topk, num_experts, _ptr(ro), _ptr(src), _ptr(pos),
+                                   _ptr(workspace), workspace.numel() * 4, flags, _stream(stream)))
     return ro, src, pos
 
 

@@ -16,71 +16,103 @@ namespace {
 constexpr int kMaxExpertsMoe = 1024;
 
 // ------------------------------------------------------------------ expert sort
-// One CTA of 1024 threads (32 warps).  Warp w owns tokens [w*tpw, (w+1)*tpw).
-//   1. per-warp expert counts (shared-memory atomics: order does not matter for counts);
-//   2. thread v turns the counts of expert v into per-warp starting rows, and a block scan over
-//      experts gives row_offsets;
-//   3. every warp walks its tokens in order, lanes = slots of one token; lanes holding the same
-//      expert (a repeated id) are ranked by slot with __match_any_sync, so the order inside an
-//      expert is (token, slot) order: a stable sort.
-// Ids outside [0, E) set bit 3 of the status word; such entries are dropped (no row, pos = -1).
-constexpr int kSortWarps = 32;
+// A stable counting sort in two kernels over G CTAs, CTA g owning tokens [g*tpc, (g+1)*tpc):
+//   1. moe_count_kernel: CTA g counts its (token, slot) pairs per expert -> hist[g][e];
+//   2. moe_place_kernel: CTA g derives, for every expert e, its first row
+//        row_offsets[e] + sum_{g' < g} hist[g'][e]   (row_offsets = prefix of the expert totals)
+//      then its 8 warps (tokens split in order between them) count again per warp, take their own
+//      first rows, and walk their tokens in order with lanes = slots; lanes holding the same expert
+//      (a repeated id) are ranked by slot with __match_any_sync.  Rows of an expert therefore keep
+//      (token, slot) order.
+// Ids outside [0, E) are dropped (pos = -1) and set bit 3 of the status word.
+constexpr int kPlaceWarps = 8;
 
-__global__ void __launch_bounds__(kSortWarps * 32) moe_sort_kernel(const int32_t *__restrict__ ids, int T, int topk,
-                                                                   int E, int64_t *__restrict__ row_offsets,
-                                                                   int32_t *__restrict__ src, int32_t *__restrict__ pos,
-                                                                   unsigned int *status) {
-  extern __shared__ int32_t cnt[];  // [kSortWarps][E]
-  __shared__ int32_t tot[kMaxExpertsMoe + 1];
+__global__ void __launch_bounds__(256) moe_count_kernel(const int32_t *__restrict__ ids, int T, int topk, int E,
+                                                        int tpc, int32_t *__restrict__ hist, unsigned int *status) {
+  extern __shared__ int32_t c[];  // [E]
+  pdl_trigger();
   pdl_wait();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  for (int i = threadIdx.x; i < kSortWarps * E; i += blockDim.x) cnt[i] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = 0;
   __syncthreads();
-  const int tpw = (T + kSortWarps - 1) / kSortWarps;
-  const int t0 = warp * tpw, t1 = min(T, t0 + tpw);
-  for (int e = t0 * topk + lane; e < t1 * topk; e += 32) {
-    const int v = ids[e];
-    if (v >= 0 && v < E) atomicAdd(&cnt[warp * E + v], 1);
+  const int t0 = blockIdx.x * tpc, t1 = min(T, t0 + tpc);
+  for (int i = t0 * topk + threadIdx.x; i < t1 * topk; i += blockDim.x) {
+    const int v = ids[i];
+    if (v >= 0 && v < E) atomicAdd(&c[v], 1);
     else atomicOr(status, 8u);
   }
   __syncthreads();
-  // per-warp exclusive offsets inside each expert, expert totals
-  for (int v = threadIdx.x; v < E; v += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < kSortWarps; ++w) {
-      const int c = cnt[w * E + v];
-      cnt[w * E + v] = run;
-      run += c;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * E + e] = c[e];
+}
+
+__global__ void __launch_bounds__(kPlaceWarps * 32) moe_place_kernel(const int32_t *__restrict__ ids, int T, int topk,
+                                                                     int E, int tpc, const int32_t *__restrict__ hist,
+                                                                     int64_t *__restrict__ row_offsets,
+                                                                     int32_t *__restrict__ src,
+                                                                     int32_t *__restrict__ pos) {
+  extern __shared__ int32_t sm[];
+  int32_t *base = sm;            // [E]: this CTA's first row per expert
+  int32_t *cnt = sm + E;         // [kPlaceWarps][E]: per-warp counts, then per-warp first rows
+  __shared__ int32_t scan[kMaxExpertsMoe];
+  pdl_trigger();
+  pdl_wait();
+  const int G = gridDim.x, g = blockIdx.x;
+  // expert totals and the part of each expert that earlier CTAs own
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+    for (int h = 0; h < G; ++h) {
+      const int v = hist[static_cast<int64_t>(h) * E + e];
+      before += h < g ? v : 0;
+      total += v;
     }
-    tot[v] = run;
+    scan[e] = total;
+    base[e] = before;
+  }
+  for (int i = threadIdx.x; i < kPlaceWarps * E; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {  // exclusive prefix of the totals (E <= 1024 adds)
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      const int v = scan[e];
+      scan[e] = acc;
+      acc += v;
+      if (g == 0) row_offsets[e] = acc - v;
+    }
+    if (g == 0) row_offsets[E] = acc;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {  // E <= 1024 sequential adds: negligible next to the rest
-    int64_t acc = 0;
-    for (int v = 0; v < E; ++v) {
-      const int c = tot[v];
-      tot[v] = static_cast<int>(acc);
-      row_offsets[v] = acc;
-      acc += c;
-    }
-    row_offsets[E] = acc;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t0 = g * tpc, t1 = min(T, t0 + tpc);
+  const int tpw = (t1 - t0 + kPlaceWarps - 1) / kPlaceWarps;
+  const int w0 = min(t1, t0 + warp * tpw), w1 = min(t1, w0 + tpw);
+  for (int i = w0 * topk + lane; i < w1 * topk; i += 32) {
+    const int v = ids[i];
+    if (v >= 0 && v < E) atomicAdd(&cnt[warp * E + v], 1);
   }
   __syncthreads();
-  for (int t = t0; t < t1; ++t) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {  // per-warp first rows inside the CTA's share
+    int run = scan[e] + base[e];
+    for (int w = 0; w < kPlaceWarps; ++w) {
+      const int v = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  for (int t = w0; t < w1; ++t) {
     const bool active = lane < topk;
     const int v = active ? ids[t * topk + lane] : -1;
     const bool ok = active && v >= 0 && v < E;
     const unsigned peers = __match_any_sync(0xFFFFFFFFu, ok ? v : -1 - lane);  // invalid lanes alone
     const int rank = __popc(peers & ((1u << lane) - 1));
-    int base = 0;
-    if (ok && rank == 0) {  // the lowest lane of each group bumps the counter for the group
-      base = cnt[warp * E + v];
-      cnt[warp * E + v] = base + __popc(peers);
+    int first = 0;
+    if (ok && rank == 0) {  // the lowest lane of each group advances the counter for the group
+      first = cnt[warp * E + v];
+      cnt[warp * E + v] = first + __popc(peers);
     }
-    base = __shfl_sync(0xFFFFFFFFu, base, __ffs(peers) - 1);
+    first = __shfl_sync(0xFFFFFFFFu, first, __ffs(peers) - 1);
     if (active) {
       if (ok) {
-        const int row = tot[v] + base + rank;
+        const int row = first + rank;
         src[row] = t;
         pos[t * topk + lane] = row;
       } else {
@@ -280,6 +312,13 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
   }
 }
 
+// CTAs of the two sort kernels: about 32 tokens each, at most 1024 (the workspace holds one
+// count per CTA and expert).
+int moe_sort_ctas(int64_t tokens) {
+  const int64_t g = ceil_div(tokens > 0 ? tokens : 1, 32);
+  return static_cast<int>(g < 1024 ? g : 1024);
+}
+
 int moe_grid(int64_t threads, int sm_count) {
   const int64_t blocks = ceil_div(threads, 256);
   const int64_t cap = static_cast<int64_t>(sm_count) * 8;
@@ -291,28 +330,42 @@ int moe_grid(int64_t threads, int sm_count) {
 
 using namespace nvfp4;
 
+extern "C" size_t moe_sort_workspace_size(int64_t num_tokens, int num_experts) {
+  if (num_tokens < 0 || num_experts < 1) return 0;
+  return static_cast<size_t>(moe_sort_ctas(num_tokens)) * num_experts * 4;
+}
+
 extern "C" nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
-                                             int64_t *row_offsets, int32_t *src_rows, int32_t *pos, uint32_t flags,
-                                             nvfp4_stream_t stream) {
+                                             int64_t *row_offsets, int32_t *src_rows, int32_t *pos, int32_t *workspace,
+                                             size_t workspace_bytes, uint32_t flags, nvfp4_stream_t stream) {
   clear_error();
   if (num_tokens < 0 || topk < 1 || topk > 32 || num_experts < 1 || num_experts > kMaxExpertsMoe ||
       num_tokens * topk >= (1LL << 31))
     return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: tokens=%lld topk=%d experts=%d (topk 1..32, experts 1..%d)",
                 (long long)num_tokens, topk, num_experts, kMaxExpertsMoe);
   if (flags & ~(uint32_t)NVFP4_FLAG_PDL) return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: unknown flags 0x%x", flags);
-  if (!row_offsets || (num_tokens > 0 && (!topk_ids || !src_rows || !pos)))
+  const size_t need = moe_sort_workspace_size(num_tokens, num_experts);
+  if (workspace_bytes < need)
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: needs a workspace of %zu bytes (got %zu)", need, workspace_bytes);
+  if (!row_offsets || !workspace || (num_tokens > 0 && (!topk_ids || !src_rows || !pos)))
     return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: null pointer");
-  if (!aligned(row_offsets, 8) || !aligned(topk_ids, 4) || !aligned(src_rows, 4) || !aligned(pos, 4))
+  if (!aligned(row_offsets, 8) || !aligned(topk_ids, 4) || !aligned(src_rows, 4) || !aligned(pos, 4) ||
+      !aligned(workspace, 4))
     return fail(NVFP4_ERR_MISALIGNED, "moe_sort_by_expert: row_offsets need 8-B, the int32 arrays 4-B alignment");
   DeviceInfo dev;
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
-  const int smem = kSortWarps * num_experts * 4;
-  st = allow_smem(reinterpret_cast<const void *>(moe_sort_kernel), smem, dev.device);
+  const int G = moe_sort_ctas(num_tokens);
+  const int tpc = static_cast<int>(ceil_div(num_tokens > 0 ? num_tokens : 1, G));
+  const int smem_count = num_experts * 4, smem_place = (1 + kPlaceWarps) * num_experts * 4;
+  st = allow_smem(reinterpret_cast<const void *>(moe_place_kernel), smem_place, dev.device);
   if (st != NVFP4_OK) return st;
-  cudaError_t e = launch(moe_sort_kernel, dim3(1), dim3(kSortWarps * 32), smem, (cudaStream_t)stream,
-                         (flags & NVFP4_FLAG_PDL) != 0, 1, topk_ids, static_cast<int>(num_tokens), topk, num_experts,
-                         row_offsets, src_rows, pos, dev.status);
+  const bool pdl = (flags & NVFP4_FLAG_PDL) != 0;
+  cudaError_t e = launch(moe_count_kernel, dim3(G), dim3(256), smem_count, (cudaStream_t)stream, pdl, 1, topk_ids,
+                         static_cast<int>(num_tokens), topk, num_experts, tpc, workspace, dev.status);
+  if (e == cudaSuccess)
+    e = launch(moe_place_kernel, dim3(G), dim3(kPlaceWarps * 32), smem_place, (cudaStream_t)stream, pdl, 1, topk_ids,
+               static_cast<int>(num_tokens), topk, num_experts, tpc, workspace, row_offsets, src_rows, pos);
   return check_launch(e, "moe_sort_by_expert");
 }
 

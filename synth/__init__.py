@@ -129,12 +129,21 @@ def weight(seed: int, n: int, k: int, std: float = 0.02, experts: int | None = N
     return to_bf16(normal(seed * 8 + STREAM_WEIGHT, count).view(shape) * std)
 
 
-def moe_routing(seed: int, tokens: int, experts: int, topk: int) -> torch.Tensor:
-    """Per-expert row counts (int64 [experts]) from softmax top-k routing of N(0,1) logits."""
+def moe_topk(seed: int, tokens: int, experts: int, topk: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """Softmax top-k routing of N(0,1) logits [tokens, experts]: (expert ids int32 [tokens, topk],
+    routing weights fp32 [tokens, topk] = the chosen probabilities renormalised to sum 1).  Ties go
+    to the lower expert id (stable sort)."""
     logits = normal(seed * 8 + STREAM_ROUTER, tokens * experts).to(torch.float32).view(tokens, experts)
     probs = torch.softmax(logits, dim=1)
-    order = torch.sort(probs, dim=1, descending=True, stable=True).indices[:, :topk]
-    return torch.bincount(order.reshape(-1), minlength=experts)
+    srt = torch.sort(probs, dim=1, descending=True, stable=True)
+    ids, p = srt.indices[:, :topk], srt.values[:, :topk]
+    return ids.to(torch.int32), (p / p.sum(dim=1, keepdim=True)).to(torch.float32)
+
+
+def moe_routing(seed: int, tokens: int, experts: int, topk: int) -> torch.Tensor:
+    """Per-expert row counts (int64 [experts]) from softmax top-k routing of N(0,1) logits."""
+    ids, _ = moe_topk(seed, tokens, experts, topk)
+    return torch.bincount(ids.to(torch.int64).reshape(-1), minlength=experts)
 
 
 def moe_offsets(counts: torch.Tensor, pad: int = 128) -> tuple[torch.Tensor, torch.Tensor]:

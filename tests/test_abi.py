@@ -137,3 +137,10 @@ def test_layout_conversion_rejects_bad_arguments_without_a_device(lib):
     # the SM103 layout is an NVFP4 layout: the MXFP4 entry points refuse the flag
     X, Q = 0x10000, 0x30000
     assert L.mxfp4_quantize(_c(X), 4, 64, 64, None, 0, _c(Q), _c(S), 1 << 20, lib.FLAG_SF_SM103, None) == 1
+
+
+def test_moe_sort_workspace_size(lib):
+    assert lib.moe_sort_workspace_size(4096, 128) == 128 * 128 * 4      # 32 tokens per CTA
+    assert lib.moe_sort_workspace_size(1, 8) == 8 * 4
+    assert lib.moe_sort_workspace_size(10 ** 6, 16) == 1024 * 16 * 4    # at most 1024 CTAs
+    assert lib.moe_sort_workspace_size(-1, 8) == 0
