@@ -226,20 +226,18 @@ __device__ __forceinline__ void bf16x8_to_f32_moe(const uint4 &v, float *f) {
   }
 }
 
-__device__ __forceinline__ int64_t sf_off_128x4(int64_t r, int64_t j, int64_t cp) {
-  return ((r >> 7) * (cp >> 2) + (j >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
-}
 
-// One thread per (scale row, scale column) of the grouped padded scale matrix: expert e owns
-// scale rows sfr[e] .. sfr[e+1]-1 (sfr[e+1] - sfr[e] = round_up(M_e, 128)); rows past an
-// expert's last token and columns past K/16 get scale 0x00.  SILU: the 16 quantised values are
+// One warp per scale row of the grouped padded scale matrix (expert e owns scale rows sfr[e] ..
+// sfr[e+1]-1, sfr[e+1] - sfr[e] = round_up(M_e, 128)), lane = scale column within a 32-column
+// pass; rows past an expert's last token and columns past K/16 get scale 0x00.  The expert of a
+// row is looked up once per warp.  SILU: the 16 quantised values are
 // h = bf16(silu(x[r, c]) * x[r, I + c]) for the block's columns c (x is [T, 2I]).
 template <bool SILU>
 __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *__restrict__ x, int64_t t,
-                                                           int64_t kb, int64_t ldx, int64_t up_off,
+                                                           int kb, int64_t ldx, int64_t up_off,
                                                            const int64_t *__restrict__ row_offsets, int experts,
                                                            const float *__restrict__ gs_e, uint8_t *__restrict__ q,
-                                                           uint8_t *__restrict__ sf, int64_t cap_rows, int64_t cp) {
+                                                           uint8_t *__restrict__ sf, int64_t cap_rows, int cp) {
   __shared__ int64_t s_ro[kMaxExpertsMoe + 1];
   __shared__ int64_t s_sfr[kMaxExpertsMoe + 1];
   pdl_trigger();
@@ -258,57 +256,63 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
   }
   __syncthreads();
   const int64_t rows = s_sfr[experts] < cap_rows ? s_sfr[experts] : cap_rows;
-  const int64_t total = rows * cp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int64_t s = idx / cp;
-    const int64_t j = idx - s * cp;
-    int lo = 0, hi = experts - 1;  // expert owning scale row s: largest e with s_sfr[e] <= s
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t wstride = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32);
+  for (int64_t srow = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + warp; srow < rows; srow += wstride) {
+    int lo = 0, hi = experts - 1;  // expert owning scale row srow: largest e with s_sfr[e] <= srow
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (s_sfr[mid] <= s) lo = mid;
+      if (s_sfr[mid] <= srow) lo = mid;
       else hi = mid - 1;
     }
-    const int64_t local = s - s_sfr[lo];
+    const int64_t local = srow - s_sfr[lo];
     const int64_t r = s_ro[lo] + local;
-    uint32_t code = 0;
-    if (local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t && j < kb) {
-      const float gs = __ldg(gs_e + lo);
-      float f[16];
-      const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
-      bf16x8_to_f32_moe(__ldg(src), f);
-      bf16x8_to_f32_moe(__ldg(src + 1), f + 8);
-      if (SILU) {
-        float u[16];
-        const uint4 *up = reinterpret_cast<const uint4 *>(x + r * ldx + up_off + j * 16);
-        bf16x8_to_f32_moe(__ldg(up), u);
-        bf16x8_to_f32_moe(__ldg(up + 1), u + 8);
+    const bool row_ok = local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t;
+    const float gs = row_ok ? __ldg(gs_e + lo) : 0.0f;
+    const __nv_bfloat16 *xrow = x + (row_ok ? r : 0) * ldx;
+    uint8_t *qrow = q + (row_ok ? r : 0) * (static_cast<int64_t>(kb) * 8);
+    uint8_t *sf_tile_row = sf + (srow >> 7) * (static_cast<int64_t>(cp) >> 2) * 512 + (srow & 31) * 16 + ((srow >> 5) & 3) * 4;
+    for (int j0 = 0; j0 < cp; j0 += 32) {  // every lane runs the same passes (shuffles below)
+      const int j = j0 + lane;
+      uint32_t code = 0;
+      if (row_ok && j < kb) {
+        float f[16];
+        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + j * 16);
+        bf16x8_to_f32_moe(__ldg(src), f);
+        bf16x8_to_f32_moe(__ldg(src + 1), f + 8);
+        if (SILU) {
+          float u[16];
+          const uint4 *up = reinterpret_cast<const uint4 *>(xrow + up_off + j * 16);
+          bf16x8_to_f32_moe(__ldg(up), u);
+          bf16x8_to_f32_moe(__ldg(up + 1), u + 8);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+          for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
+        code = e4m3_code(sc);
+        const float sd = e4m3_value(code);
+        const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
+        float y0[8], y1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          y0[i] = __fmul_rn(f[i], inv);
+          y1[i] = __fmul_rn(f[8 + i], inv);
+        }
+        uint2 out;
+        out.x = e2m1x8(y0);
+        out.y = e2m1x8(y1);
+        *reinterpret_cast<uint2 *>(qrow + j * 8) = out;
       }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
-      code = e4m3_code(sc);
-      const float sd = e4m3_value(code);
-      const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
-      float y0[8], y1[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y0[i] = __fmul_rn(f[i], inv);
-        y1[i] = __fmul_rn(f[8 + i], inv);
-      }
-      uint2 out;
-      out.x = e2m1x8(y0);
-      out.y = e2m1x8(y1);
-      *reinterpret_cast<uint2 *>(q + r * (kb * 8) + j * 8) = out;
+      // 4 lanes (scale columns 4c .. 4c+3 of the row) -> one 32-bit word of the 128x4 layout
+      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
+      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+      if ((j & 3) == 0 && j < cp)
+        *reinterpret_cast<uint32_t *>(sf_tile_row + (j >> 2) * 512) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
     }
-    // 4 lanes (scale columns 4c .. 4c+3, adjacent positions of one row) -> one 32-bit word
-    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
-    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
-    if ((j & 3) == 0) *reinterpret_cast<uint32_t *>(sf + sf_off_128x4(s, j, cp)) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
   }
 }
 
@@ -418,7 +422,7 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
                             const int64_t *row_offsets, int num_experts, const float *gs, uint8_t *q, uint8_t *sf,
                             size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream) {
   clear_error();
-  if (t < 0 || k <= 0) return fail(NVFP4_ERR_INVALID_ARG, "%s: t=%lld k=%lld", name, (long long)t, (long long)k);
+  if (t < 0 || k <= 0 || k >= (1LL << 31)) return fail(NVFP4_ERR_INVALID_ARG, "%s: t=%lld k=%lld", name, (long long)t, (long long)k);
   if (k % 16) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: k=%lld is not a multiple of 16", name, (long long)k);
   const int64_t width = silu ? 2 * k : k;
   if (ldx < width || ldx % 8)
@@ -438,11 +442,12 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
-  const int64_t total = (round_up(t, 128) + 128LL * num_experts) * cp;
+  const int64_t scale_rows = round_up(t, 128) + 128LL * num_experts;  // bound of sum_e round_up(M_e, 128)
   auto kern = silu ? expert_quant_kernel<true> : expert_quant_kernel<false>;
-  cudaError_t e = launch(kern, dim3(moe_grid(total, dev.sm_count)), dim3(256), 0, (cudaStream_t)stream,
-                         (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x), t, k / 16, ldx,
-                         silu ? k : static_cast<int64_t>(0), row_offsets, num_experts, gs, q, sf, cap_rows, cp);
+  cudaError_t e = launch(kern, dim3(moe_grid(scale_rows * 32, dev.sm_count)), dim3(256), 0, (cudaStream_t)stream,
+                         (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x), t,
+                         static_cast<int>(k / 16), ldx, silu ? k : static_cast<int64_t>(0), row_offsets, num_experts,
+                         gs, q, sf, cap_rows, static_cast<int>(cp));
   return check_launch(e, name);
 }
 }  // namespace
