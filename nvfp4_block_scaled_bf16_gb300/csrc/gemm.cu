@@ -15,9 +15,10 @@
 //             its ring the operands land with few copies ("resident"), and at most 3 stages per
 //             CTA are in flight: with cold HBM, requesting every stage at once made all of them
 //             land together, leaving no load for the MMAs to overlap.
-//   M >  256  128 x 256 tiles (128 x 128 when N is not a multiple of 256 or there are fewer
-//             256-wide tiles than SMs), persistent over the SMs, double-buffered accumulators
-//             where tensor memory allows.  When the tiles fill less than half the SMs and K is
+//   M >  256  256 x 256 tiles computed by CTA pairs (cta_group::2) when N is a multiple of 256
+//             and there are at least as many 128 x 256 tiles as SMs; otherwise 128 x 128 tiles on
+//             single CTAs.  Persistent over the SMs, double-buffered accumulators where tensor
+//             memory allows (128 x 128).  When the tiles fill less than half the SMs and K is
 //             long (>= 4 K stages per SM), the (tile, K stage) units are split stream-K over all
 //             SMs and split tiles are added up through the workspace.  Splitting the last wave of
 //             large shapes the same way was measured slower: every SM is already bound by its
@@ -30,6 +31,7 @@ namespace {
 
 struct Plan {
   int swap, bn, splits, stages, ctas, m_tiles, n_tiles, k_tiles, dp_tiles, sk_tiles;
+  int pair;  // 1: 256 x 256 tiles computed by CTA pairs (cta_group::2); m_tiles counts 256 rows
   int resident, nst_max, lookahead;  // see GemmArgs
   size_t ws_bytes;
 };
@@ -69,11 +71,19 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   } else {
     pl.swap = 0;
     pl.bn = (n % 256 == 0 && ceil_div(m, 128) * (n / 256) >= sm_count) ? 256 : 128;
-    pl.m_tiles = static_cast<int>(ceil_div(m, 128));
+    // 256-wide tiles go to CTA pairs: a single CTA's 128 x 256 tile moves 54 KB through shared
+    // memory per K stage (TMA writes, MMA reads, scale reads) and is bound by that bandwidth; a
+    // pair stages half of B per CTA.
+    pl.pair = pl.bn == 256 ? 1 : 0;
+    pl.m_tiles = static_cast<int>(ceil_div(m, pl.pair ? 256 : 128));
     pl.n_tiles = static_cast<int>(ceil_div(n, pl.bn));
     const int tiles = pl.m_tiles * pl.n_tiles;
     const int64_t units = static_cast<int64_t>(tiles) * pl.k_tiles;
-    if (2 * tiles <= sm_count && units >= 4LL * sm_count) {
+    if (pl.pair) {
+      const int pairs = sm_count / 2;
+      pl.dp_tiles = tiles;
+      pl.ctas = 2 * (tiles < pairs ? tiles : pairs);
+    } else if (2 * tiles <= sm_count && units >= 4LL * sm_count) {
       // few tiles with a long K: whole tiles would leave most SMs idle
       pl.sk_tiles = tiles;
       pl.ctas = sm_count;
@@ -100,7 +110,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     case 32: pl.stages = 4; break;
     case 64: pl.stages = 7; break;
     case 128: pl.stages = 6; break;
-    default: pl.stages = 4; break;
+    default: pl.stages = pl.pair ? 6 : 4; break;
   }
   // A swap-AB CTA holds one tile; when its whole K slice fits the ring (and K is a whole number of
   // 256-wide stages), the activation and both scale slices land with one copy each.
@@ -131,7 +141,8 @@ nvfp4_status_t with_config(const Plan &pl, F &&f) {
     case 32: return f(GemmCfg<32, 4, false, false, 2>{});
     case 64: return f(GemmCfg<64, 7, false, false>{});
     case 128: return pl.swap ? f(GemmCfg<128, 6, false, false>{}) : f(GemmCfg<128, 6, false, true>{});
-    default: return pl.swap ? f(GemmCfg<256, 4, false, false>{}) : f(GemmCfg<256, 4, false, true>{});
+    default:
+      return pl.swap ? f(GemmCfg<256, 4, false, false>{}) : f(GemmCfg<256, 6, false, true, 1, true>{});
   }
 }
 
@@ -151,7 +162,7 @@ extern "C" nvfp4_status_t nvfp4_gemm_plan(int64_t m, int64_t n, int64_t k, nvfp4
   if (!plan || m < 0 || n <= 0 || k <= 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm_plan: bad arguments");
   const Plan pl = select_plan(m, n, k, plan_sm_count());
   plan->swap_ab = pl.swap;
-  plan->tile_m = 128;
+  plan->tile_m = pl.pair ? 256 : 128;
   plan->tile_n = pl.bn;
   plan->splits = pl.splits;
   plan->stages = pl.stages;
@@ -203,7 +214,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   CUtensorMap ta, tb, tb3;
   st = encode_tmap_2d_u8(&ta, opa, k / 2, rows_a, k / 2, 128, 128, true);
   if (st != NVFP4_OK) return st;
-  st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.bn, true);
+  st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.pair ? pl.bn / 2 : pl.bn, true);
   if (st != NVFP4_OK) return st;
   if (pl.resident) {
     st = encode_tmap_stages_u8(&tb3, opb, k / 2, rows_b, pl.bn, pl.nst_max);
@@ -248,7 +259,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   return with_config(pl, [&](auto cfg) {
     using C = decltype(cfg);
     const cudaError_t e = launch(bs_gemm_kernel<C, false>, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
-                                 (flags & NVFP4_FLAG_PDL) != 0, pl.splits, ta, tb, tb3, args);
+                                 (flags & NVFP4_FLAG_PDL) != 0, pl.pair ? 2 : pl.splits, ta, tb, tb3, args);
     return check_launch(e, "nvfp4_gemm");
   });
 }

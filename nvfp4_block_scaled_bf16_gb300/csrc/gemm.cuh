@@ -30,8 +30,20 @@
 //               128x256x64 MMA).
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
 //
+// CTA pairs (PAIR, 256 x 256 tiles for large M): a cluster of two CTAs runs cta_group::2 MMAs
+// (M = 256, issued by the first CTA; a 256x256x64 MMA occupies the pipe for the same ~128 cycles
+// as a 128x256x64 one on a single CTA).  Each CTA stages its 128 rows of A and its 128 rows of B;
+// the scales of its A rows and of all 256 B rows go through a separate 5-slot ring that warp 10
+// fills ahead of the operands, so the producer issues two copies per stage.  The hand-offs
+// across the pair: the second CTA's MMA warp (which issues no MMAs) relays "stage landed", its
+// scale writers and epilogue arrive on the first CTA's barriers, and the first CTA's commits
+// arrive on both CTAs' barriers (multicast).  Arrivals use the default CTA-scope release: a
+// cluster-scope release measured 1000-1500 cycles per arrive; every arrival follows the
+// completion of what it announces (tcgen05.wait::st / ::ld, a completed barrier).
+//
 // Work decomposition: each CTA walks a list of segments (tile, K-stage range).
-//   - whole tiles: CTA c takes tiles c, c+G, c+2G, ... below dp_tiles (G = grid size);
+//   - whole tiles: CTA c takes tiles c, c+G, c+2G, ... below dp_tiles (G = grid size; for
+//     pairs, cluster c of G/2);
 //   - stream-K: the (tile, K stage) units of the sk_tiles tiles after them are cut into G
 //     contiguous runs of equal length, one per CTA.  A run that covers only part of a tile
 //     stores its fp32 partial tile in a workspace slot; the last CTA to finish the tile (an
@@ -60,7 +72,7 @@ enum : int {
   kSiteEpilogue = 6     // epilogue: accumulator complete
 };
 
-template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1>
+template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1, bool PAIR_ = false>
 struct GemmCfg {
   static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
   static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
@@ -72,13 +84,21 @@ struct GemmCfg {
   // CTAs per SM the registers are budgeted for (2: consecutive GEMMs of a PDL chain can share
   // the SMs, the next one streaming its weights while this one finishes)
   static constexpr int MIN_BLOCKS = MIN_BLOCKS_;
-  static constexpr int BM = 128;          // MMA M: rows of operand A per tile
+  // PAIR: a cluster of two CTAs computes one 256 x BN tile with cta_group::2 MMAs issued by the
+  // first CTA.  Each CTA stages 128 rows of A and BN/2 rows of B (the MMA reads the other half
+  // of B from the peer's shared memory) plus the scales of its A rows and of all BN B rows, and
+  // holds its 128 rows of the accumulator.  Per K stage an SM then moves 38 KB through shared
+  // memory instead of 54 KB, and shared-memory bandwidth is what bounds the single-CTA tile.
+  static constexpr bool PAIR = PAIR_;
+  static constexpr int CG = PAIR ? 2 : 1;
+  static constexpr int BM = 128;          // MMA M: rows of operand A per tile (per CTA)
   static constexpr int KSTAGE = 256;      // K elements per stage = one 128-byte TMA row
   static constexpr int VEC = MX ? 32 : 16;
   static constexpr int CHUNKS = KSTAGE / VEC / 4;  // 512-byte scale chunks per 128 rows per stage
   static constexpr int SFB_BLOCKS = (BN + 127) / 128;
   static constexpr int A_BYTES = BM * 128;
-  static constexpr int B_BYTES = BN * 128;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of operand B a CTA stages
+  static constexpr int B_BYTES = B_ROWS * 128;
   static constexpr int SFA_BYTES = CHUNKS * 512;
   static constexpr int SFB_BYTES = SFB_BLOCKS * CHUNKS * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -98,27 +118,37 @@ struct GemmCfg {
   static constexpr int MAX_EXPERTS = 1024;
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
   static constexpr int CTRL_BYTES = 512;
-  static constexpr int THREADS = 320;
+  // A pair adds warp 10, which copies the scales into a ring of their own (SF_STAGES deep) ahead
+  // of the operands, so that writing them to tensor memory is off the operand ring's critical
+  // path and the producer issues two copies per stage instead of five.
+  static constexpr int SF_STAGES = PAIR ? 5 : STAGES;
+  static constexpr int THREADS = PAIR ? 352 : 320;
   // The ring keeps each operand in a region of its own (stage i of A at A_REGION + i * A_BYTES,
   // and so on), so the stages of one operand are contiguous and a CTA whose whole K slice fits
   // the ring can land an operand's slice with a single copy.
-  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES) + SF_STAGES * (SFA_BYTES + SFB_BYTES);
   static constexpr int B_REGION = STAGES * A_BYTES;
   static constexpr int SFA_REGION = B_REGION + STAGES * B_BYTES;
-  static constexpr int SFB_REGION = SFA_REGION + STAGES * SFA_BYTES;
+  static constexpr int SFB_REGION = SFA_REGION + SF_STAGES * SFA_BYTES;
   // dynamic shared memory: alignment slack, stage ring, barriers, expert tables (grouped only)
   static constexpr int smem_bytes(bool grouped) {
     return 1024 + RING_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
   }
-  static constexpr uint32_t IDESC = idesc_block_scaled(BM, BN, MX, 0);
+  static constexpr uint32_t IDESC = idesc_block_scaled(PAIR ? 2 * BM : BM, BN, MX, 0);
+  // arrivals on the scale-slot-written and accumulator-drained barriers (both CTAs of a pair
+  // arrive on the first CTA's)
+  static constexpr int SLOT_ARRIVALS = PAIR ? 8 : 4;
+  static constexpr int ACC_ARRIVALS = PAIR ? 8 : 4;
   static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8, "tensor memory budget, scale-slot barriers");
-  static_assert((2 * STAGES + 22) * 8 + 7 * 4 <= CTRL_BYTES, "barriers and flags fit the control block");
+  static_assert(STAGES <= 8 && SF_STAGES <= 8 && (2 * STAGES + 45) * 8 + 8 * 4 <= CTRL_BYTES,
+                "barriers and flags fit the control block");
   static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
   static_assert(MIN_BLOCKS == 1 || (MIN_BLOCKS * (smem_bytes(false) + 1024) <= 233472 && MIN_BLOCKS * TMEM_COLS <= 512),
                 "shared and tensor memory for MIN_BLOCKS CTAs per SM");
-  static_assert(RED_BYTES <= STAGES * STAGE_BYTES, "split-K buffer must fit in the stage ring");
+  static_assert(RED_BYTES <= RING_BYTES, "split-K buffer must fit in the stage ring");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
+  static_assert(!PAIR || (MULTI_TILE && BN == 256 && !MX), "CTA pairs: NVFP4 256-wide whole tiles only");
 };
 
 struct GemmArgs {
@@ -215,7 +245,8 @@ struct Work {
   }
 };
 
-template <bool GROUPED>
+// PAIR: the two CTAs of a cluster walk the same tiles (cluster c takes tiles c, c+G/2, ...).
+template <bool GROUPED, bool PAIR = false>
 __device__ __forceinline__ Work make_work(const GemmArgs &p, int grouped_tiles) {
   Work w{};
   w.kt_lo = 0;
@@ -224,8 +255,8 @@ __device__ __forceinline__ Work make_work(const GemmArgs &p, int grouped_tiles) 
   w.splits = 1;
   w.u = w.u_end = 0;
   w.units = 1;
-  w.tile = blockIdx.x;
-  w.tile_step = gridDim.x;
+  w.tile = PAIR ? blockIdx.x >> 1 : blockIdx.x;
+  w.tile_step = PAIR ? gridDim.x >> 1 : gridDim.x;
   if (GROUPED) {
     w.tile_end = grouped_tiles;
   } else if (p.splits > 1) {
@@ -254,11 +285,28 @@ struct Tables {
   int *tp;   // [experts+1] tile prefix
 };
 
+// rank: this CTA's place in its pair (PAIR only).
 template <class C, bool GROUPED>
-__device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C, GROUPED> &tb, int tile) {
+__device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C, GROUPED> &tb, int tile, int rank = 0) {
   TileInfo t;
   int64_t sfb_base_block;
-  if constexpr (GROUPED) {
+  if constexpr (C::PAIR) {
+    // 256 x BN tiles (m_tiles counts 256-row tiles); CTA `rank` holds rows 128*rank .. +127 of
+    // the tile and rows B_ROWS*rank .. +B_ROWS-1 of its B block.  A CTA wholly past the last
+    // row stages zero-filled A and the tile's first scale block, and stores nothing.
+    const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+    t.a_y = mb * 2 * C::BM + C::BM * rank;
+    t.b_y = nb * C::BN + C::B_ROWS * rank;
+    t.rows = max(0, min(C::BM, p.m - t.a_y));
+    const int sfa_block = t.rows > 0 ? 2 * mb + rank : 2 * mb;
+    t.sfa_blk = p.sfa + static_cast<int64_t>(sfa_block) * p.sf_chunks * 512;
+    sfb_base_block = (nb * C::BN) / 128;
+    t.sfb_blk = p.sfb + sfb_base_block * p.sf_chunks * 512;
+    t.cols = min(C::BN, p.n - nb * C::BN);
+    t.out_i0 = t.a_y;
+    t.out_j0 = nb * C::BN;
+    t.expert = 0;
+  } else if constexpr (GROUPED) {
     int lo = 0, hi = p.experts - 1;  // largest e with tp[e] <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -317,15 +365,24 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
   const uint32_t bar = smem_u32(&full[stg]);
   if (do_a) {
     tma_load_2d(smem_u32(smem + stg * C::A_BYTES), tmA, bar, kt * 128, t.a_y);
-    bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES), t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512,
-              nch * 512, bar);
+    if constexpr (!C::PAIR)  // (a pair's scales go through their own ring)
+      bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES),
+                t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
   }
   if (do_b) {
     tma_load_2d(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt * 128, t.b_y);
-    for (int b = 0; b < t.sfb_blocks; ++b)
-      bulk_load(smem_u32(smem + C::SFB_REGION + stg * C::SFB_BYTES + b * C::CHUNKS * 512),
-                t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+    if constexpr (!C::PAIR)
+      for (int b = 0; b < t.sfb_blocks; ++b)
+        bulk_load(smem_u32(smem + C::SFB_REGION + stg * C::SFB_BYTES + b * C::CHUNKS * 512),
+                  t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
   }
+}
+
+// Bytes that land on full[] for K stage kt (operands, and scales unless they have their own ring).
+template <class C>
+__device__ __forceinline__ uint32_t stage_tx(const GemmArgs &p, const TileInfo &t, int kt) {
+  if constexpr (C::PAIR) return C::A_BYTES + C::B_BYTES;
+  else return C::A_BYTES + C::B_BYTES + stage_chunks<C>(p, kt) * 512 * (1 + t.sfb_blocks);
 }
 
 // Stream-K partial tiles.  A slot holds one CTA's fp32 partial of a 128 x BN tile in chunk-row
@@ -346,7 +403,7 @@ __device__ __forceinline__ float *sk_slot(const GemmArgs &p, int cta, int j) {
 template <class C>
 __device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, const Seg &s, float alpha, int tid,
                                          uint8_t *smem) {
-  constexpr int RING = C::STAGES * C::STAGE_BYTES;
+  constexpr int RING = C::RING_BYTES;
   constexpr int CHUNK_BYTES = 128 * 32 * 4;  // one 32-column chunk of a partial
   if (s.n * CHUNK_BYTES > RING) {  // never planned (the host caps contributors); uniform exit
     if (tid == 0) atomicOr(p.status, 4u);
@@ -406,8 +463,16 @@ __device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, c
   }
 }
 
+// Arrive on `bar` once the calling thread's tcgen05 operations so far are complete; for a CTA
+// pair, on the barrier at that offset in both CTAs.
+template <class C>
+__device__ __forceinline__ void commit_to(uint32_t bar) {
+  if constexpr (C::PAIR) tc_commit_pair_mc(bar, static_cast<uint16_t>(0x3));
+  else tc_commit(bar);
+}
+
 template <class C, bool GROUPED>
-__global__ void __launch_bounds__(320, C::MIN_BLOCKS)
+__global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -420,16 +485,21 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
   uint64_t *sff = acce + 2;           // scale slot written (4 scale-writer warps arrive)
   uint64_t *sfe = sff + 8;            // scale slot free (MMA commit)
   uint64_t *drain = sfe + 8;
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *sf_full = drain + 1;       // pair: scale ring slot landed
+  uint64_t *sf_empty = sf_full + 8;    // pair: scale ring slot read by the 4 scale writers
+  uint64_t *peer_full = sf_empty + 8;  // pair (first CTA): the second CTA's operand stage landed
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(peer_full + 8);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
   volatile int *issued_count = consumed + 1;  // K stages the producer issued (abort drain)
   volatile int *sk_last = consumed + 2;       // stream-K: epilogue decision broadcast
   volatile float *alpha_s = reinterpret_cast<volatile float *>(sk_last + 1);  // alpha, read once
+  volatile int *sf_issued = reinterpret_cast<volatile int *>(alpha_s + 1);   // pair: scale stages issued
   int *tables = reinterpret_cast<int *>(ctrl + C::CTRL_BYTES);
   Tables<C, GROUPED> tb{tables, tables + (C::MAX_EXPERTS + 1), tables + 2 * (C::MAX_EXPERTS + 1)};
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int crank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // place in the CTA pair
   const WaitCtl wc{p.wait_limit, abort_flag, p.status};
   // The next kernel may launch now: it waits (griddepcontrol.wait) for this grid to complete
   // before it reads our output, and its CTAs can meanwhile take the SM space we leave free.
@@ -442,13 +512,21 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&accf[a]), 1);
-      mbar_init(smem_u32(&acce[a]), 4);
+      mbar_init(smem_u32(&acce[a]), C::ACC_ARRIVALS);
     }
     for (int q = 0; q < C::SF_SLOTS; ++q) {
-      mbar_init(smem_u32(&sff[q]), 4);
+      mbar_init(smem_u32(&sff[q]), C::SLOT_ARRIVALS);
       mbar_init(smem_u32(&sfe[q]), 1);
     }
     mbar_init(smem_u32(drain), 1);
+    if constexpr (C::PAIR) {
+      for (int j = 0; j < C::SF_STAGES; ++j) {
+        mbar_init(smem_u32(&sf_full[j]), 1);
+        mbar_init(smem_u32(&sf_empty[j]), 4);
+      }
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&peer_full[s]), 1);
+    }
+    *sf_issued = 0;
     *abort_flag = 0;
     *consumed = 0;
     *issued_count = 0;
@@ -512,15 +590,18 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     }
   }
 
-  __syncthreads();  // barriers initialised (and expert tables written, grouped)
-  const Work work0 = make_work<GROUPED>(p, GROUPED ? tb.tp[p.experts] : 0);
+  // barriers initialised (and expert tables written, grouped); a pair's CTAs arrive on each
+  // other's barriers, so both must have initialised theirs
+  if constexpr (C::PAIR) cluster_sync();
+  else __syncthreads();
+  const Work work0 = make_work<GROUPED, C::PAIR>(p, GROUPED ? tb.tp[p.experts] : 0);
   // The loader (warp 0) starts right away; warp 1 allocates tensor memory meanwhile and a named
   // barrier among warps 1..9 (the tensor-memory users) publishes its address.
   uint32_t tmem = 0;
   if (warp != 0) {
     if (warp == 1) {
-      tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
-      tmem_relinquish();
+      tmem_alloc<C::CG>(smem_u32(tmem_holder), C::TMEM_COLS);
+      tmem_relinquish<C::CG>();
     }
     tc_fence_before();
     named_barrier_sync(1, C::THREADS - 32);
@@ -537,7 +618,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         // Everything but B's half (the activation, under PDL) went out during set-up.
         Seg s0;
         if (Work(work0).next(p, s0)) {
-          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile, crank);
           if (p.weight_operand == 1) {
             pdl_wait();
             tma_load_3d(smem_u32(smem + C::B_REGION), &tmB3, smem_u32(&full[0]), 0, t.b_y, s0.kt0);
@@ -564,12 +645,11 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         Work w = work0;
         Seg s0;
         if (!GROUPED && (pre_a || pre_b) && Work(work0).next(p, s0)) {
-          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile);
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile, crank);
           pre = min(p.lookahead > 0 ? p.lookahead : C::STAGES, min(C::STAGES, s0.kt1 - s0.kt0));
           for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
             const int kt = s0.kt0 + i;
-            const int nch = stage_chunks<C>(p, kt);
-            mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+            mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx<C>(p, t, kt));
             if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
           }
           if (C::SWAP_ONLY && pre_a) {
@@ -584,7 +664,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         pdl_wait();
         bool first = true;
         for (Seg sg; w.next(p, sg); first = false) {
-          const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+          const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
           for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
             const bool early_stage = first && kt - sg.kt0 < pre;
             if (p.lookahead > 0 && issued >= p.lookahead) {  // pacing: stage issued - L has landed
@@ -592,9 +672,8 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
               if (!mbar_wait(smem_u32(&full[j % C::STAGES]), (j / C::STAGES) & 1, wc, kSiteLoadEmpty)) goto producer_done;
             }
             if (!early_stage) {
-              if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) goto producer_done;
-              const int nch = stage_chunks<C>(p, kt);
-              mbar_arrive_expect_tx(smem_u32(&full[stage]), C::A_BYTES + C::B_BYTES + nch * 512 * (1 + t.sfb_blocks));
+              if (!mbar_wait<C::PAIR>(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) goto producer_done;
+              mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx<C>(p, t, kt));
             }
             const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
             if (!(skip_first && issued == 0) && (do_a || do_b))
@@ -636,31 +715,57 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
           const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + C::B_REGION + i * C::B_BYTES));
           const uint32_t sb = slot + C::SFA_COLS;
           constexpr uint32_t SB = 4 * C::SFB_BLOCKS;
+          // (resident CTAs are swap-AB, never pairs; the group template only keeps every
+          // tcgen05 instruction of a pair kernel in the same CTA group)
           if constexpr (!C::MX) {
-            mma_nvf4(tmem, adesc, bdesc, C::IDESC, slot, sb, i > 0 ? 1u : 0u);
-            mma_nvf4(tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
-            mma_nvf4(tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
-            mma_nvf4(tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
+            mma_nvf4<C::CG>(tmem, adesc, bdesc, C::IDESC, slot, sb, i > 0 ? 1u : 0u);
+            mma_nvf4<C::CG>(tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
+            mma_nvf4<C::CG>(tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
+            mma_nvf4<C::CG>(tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
           }
         }
-        tc_commit(smem_u32(&accf[0]));
+        tc_commit<C::CG>(smem_u32(&accf[0]));
       }
     mma_done_r:
       *consumed = taken;
-    } else if (lane == 0) {
+    } else if (C::PAIR && lane == 0 && crank == 1) {
+      // Relay of the pair's second CTA (which issues no MMAs): tells the first CTA's MMA lane
+      // when each operand stage of this CTA has landed.
       int stage = 0;
+      uint32_t phase = 0;
+      Work w = work0;
+      for (Seg sg; w.next(p, sg);) {
+        for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteMmaFull)) goto relay_done;
+          mbar_arrive_remote(map_to_rank(smem_u32(&peer_full[stage]), 0));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    relay_done:;
+    } else if (lane == 0 && crank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;  // of full[] / peer_full[] (pairs wait on them; others rely on sff)
       int taken = 0;  // stages known landed (abort drain)
       int acc = 0;
       uint32_t acc_phase = 0;
       uint32_t it = 0;
       Work w = work0;
       for (Seg sg; w.next(p, sg);) {
-        if (!mbar_wait(smem_u32(&acce[acc]), acc_phase ^ 1, wc, kSiteMmaAcc)) goto mma_done;
+        if (!mbar_wait<C::PAIR>(smem_u32(&acce[acc]), acc_phase ^ 1, wc, kSiteMmaAcc)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * C::BN;
         for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
           const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-          if (!mbar_wait(smem_u32(&sff[s_idx]), s_round & 1, wc, kSiteMmaScale)) goto mma_done;
+          if (!mbar_wait<C::PAIR>(smem_u32(&sff[s_idx]), s_round & 1, wc, kSiteMmaScale)) goto mma_done;
+          if constexpr (C::PAIR) {
+            // a pair's scale writers do not wait for the operands: the stage's A and B halves
+            // of both CTAs are waited for here
+            if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteMmaFull)) goto mma_done;
+            if (!mbar_wait<true>(smem_u32(&peer_full[stage]), phase, wc, kSiteMmaFull)) goto mma_done;
+          }
           ++taken;
           tc_fence_after();
           const uint32_t slot = tmem + C::SF_COL0 + s_idx * C::SF_SLOT;
@@ -687,20 +792,24 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
             const uint32_t sb = slot + C::SFA_COLS;
             constexpr uint32_t SB = 4 * C::SFB_BLOCKS;  // B scale columns per MMA
             if (stage_mmas(p, kt) == 4) {
-              mma_nvf4(d_tmem, adesc, bdesc, C::IDESC, slot, sb, acc0);
-              mma_nvf4(d_tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
-              mma_nvf4(d_tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
-              mma_nvf4(d_tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
+              mma_nvf4<C::CG>(d_tmem, adesc, bdesc, C::IDESC, slot, sb, acc0);
+              mma_nvf4<C::CG>(d_tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
+              mma_nvf4<C::CG>(d_tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
+              mma_nvf4<C::CG>(d_tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
             } else {
               for (int j = 0; j < stage_mmas(p, kt); ++j)
-                mma_nvf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB, j > 0 ? 1u : acc0);
+                mma_nvf4<C::CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB,
+                                j > 0 ? 1u : acc0);
             }
           }
-          tc_commit(smem_u32(&empty[stage]));
-          tc_commit(smem_u32(&sfe[s_idx]));
-          if (++stage == C::STAGES) stage = 0;
+          commit_to<C>(smem_u32(&empty[stage]));
+          commit_to<C>(smem_u32(&sfe[s_idx]));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
-        tc_commit(smem_u32(&accf[acc]));
+        commit_to<C>(smem_u32(&accf[acc]));
         if (++acc == C::NACC) {
           acc = 0;
           acc_phase ^= 1;
@@ -709,7 +818,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     mma_done:
       *consumed = taken;
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ------------------------------------------------------------ scale writers
     // Each warp fills its own 32-lane quadrant of the slot with the full scale data of the
     // stage (the MMA reads every quadrant): lane i takes bytes 16*i .. 16*i+15 of every
@@ -759,10 +868,16 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     for (Seg sg; w.next(p, sg);) {
       for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
         const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-        if (!mbar_wait(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc, kSiteScaleSlot)) goto scale_done;
-        if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
-        const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + stage * C::SFA_BYTES);
-        const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + stage * C::SFB_BYTES);
+        if (!mbar_wait<C::PAIR>(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc, kSiteScaleSlot)) goto scale_done;
+        // The stage's scales land with its operands, or (pair) in the scale ring ahead of them.
+        const int sf_slot = C::PAIR ? static_cast<int>(it % C::SF_STAGES) : stage;
+        if constexpr (C::PAIR) {
+          if (!mbar_wait(smem_u32(&sf_full[sf_slot]), (it / C::SF_STAGES) & 1, wc, kSiteScaleFull)) goto scale_done;
+        } else {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
+        }
+        const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + sf_slot * C::SFA_BYTES);
+        const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + sf_slot * C::SFB_BYTES);
         uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
@@ -784,10 +899,17 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         const uint32_t slot = tmem + lane_base + C::SF_COL0 + s_idx * C::SF_SLOT;
         tmem_st_32x32b<C::SFA_COLS>(slot, ra);
         tmem_st_32x32b<C::SFB_COLS>(slot + C::SFA_COLS, rb);
+        if constexpr (C::PAIR) {  // the scales are in registers: the ring slot may be refilled
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sf_empty[sf_slot]));
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sff[s_idx]));
+        if (lane == 0) {
+          if constexpr (C::PAIR) mbar_arrive_remote(map_to_rank(smem_u32(&sff[s_idx]), 0));
+          else mbar_arrive(smem_u32(&sff[s_idx]));
+        }
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
@@ -795,6 +917,32 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
       }
     }
   scale_done:;
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ scale copies (pairs only)
+    // One thread fills the scale ring: both scale slices of each K stage, as far ahead of the
+    // scale writers as the ring allows.
+    if (lane == 0) {
+      pdl_wait();  // the activation's scales may come from the preceding kernel
+      int it = 0;
+      Work w = work0;
+      for (Seg sg; w.next(p, sg);) {
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
+        for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
+          const int j = it % C::SF_STAGES;
+          if (!mbar_wait(smem_u32(&sf_empty[j]), ((it / C::SF_STAGES) & 1) ^ 1, wc, kSiteLoadEmpty)) goto sfcopy_done;
+          const int nch = stage_chunks<C>(p, kt);
+          const uint32_t bar = smem_u32(&sf_full[j]);
+          mbar_arrive_expect_tx(bar, nch * 512 * (1 + t.sfb_blocks));
+          bulk_load(smem_u32(smem + C::SFA_REGION + j * C::SFA_BYTES),
+                    t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
+          for (int b = 0; b < t.sfb_blocks; ++b)
+            bulk_load(smem_u32(smem + C::SFB_REGION + j * C::SFB_BYTES + b * C::CHUNKS * 512),
+                      t.sfb_blk + (static_cast<int64_t>(b) * p.sf_chunks + kt * C::CHUNKS) * 512, nch * 512, bar);
+          *sf_issued = it + 1;
+        }
+      }
+    sfcopy_done:;
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     pdl_wait();
@@ -810,7 +958,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
       Work w = work0;
       Seg sg{};
       if (w.next(p, sg)) {
-        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
         if (row < t.rows) {
           if (p.swap) {
             prefetch_l2(p.d + t.out_j0 * p.ldd + t.out_i0 + row);
@@ -831,9 +979,9 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     // After a failed wait the warps keep walking the segments without doing work (every later
     // wait returns at once), so all four always meet the same named barriers.
     for (Seg sg; w.next(p, sg);) {
-      const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+      const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
       const bool sk_part = C::MULTI_TILE && !GROUPED && p.splits == 1 && sg.n > 1;
-      const bool ok = mbar_wait(smem_u32(&accf[acc]), acc_phase, wc, kSiteEpilogue);
+      const bool ok = mbar_wait<C::PAIR>(smem_u32(&accf[acc]), acc_phase, wc, kSiteEpilogue);
       tc_fence_after();
       const uint32_t t_base = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * C::BN;
       const float tile_alpha = (GROUPED && p.alpha_per_expert && p.alpha) ? __ldg(p.alpha + t.expert) : alpha;
@@ -883,7 +1031,10 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce[acc]));
+      if (lane == 0) {
+        if constexpr (C::PAIR) mbar_arrive_remote(map_to_rank(smem_u32(&acce[acc]), 0));
+        else mbar_arrive(smem_u32(&acce[acc]));
+      }
       if (++acc == C::NACC) {
         acc = 0;
         acc_phase ^= 1;
@@ -922,7 +1073,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
       named_barrier_sync(2, 128);
       if (tid == 0) *sk_last = *abort_flag ? -1 : 1;  // after a time-out copies may still land in the ring
       named_barrier_sync(2, 128);
-      if (*sk_last == 1) sk_fixup<C>(p, tile_info<C, GROUPED>(p, tb, pending.tile), pending, alpha, tid, smem);
+      if (*sk_last == 1) sk_fixup<C>(p, tile_info<C, GROUPED>(p, tb, pending.tile, crank), pending, alpha, tid, smem);
     }
   }
 
@@ -940,9 +1091,18 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         while (!mbar_try_wait(bar, (i / C::STAGES) & 1) && clock64() - t0 < p.wait_limit) {
         }
       }
+      if constexpr (C::PAIR) {  // and the scale ring's copies
+        const int sfi = *sf_issued;
+        for (int i = sfi > C::SF_STAGES ? sfi - C::SF_STAGES : 0; i < sfi; ++i) {
+          const uint32_t bar = smem_u32(&sf_full[i % C::SF_STAGES]);
+          const long long t0 = clock64();
+          while (!mbar_try_wait(bar, (i / C::SF_STAGES) & 1) && clock64() - t0 < p.wait_limit) {
+          }
+        }
+      }
     }
     if (threadIdx.x == 32) {
-      tc_commit(smem_u32(drain));
+      tc_commit<C::CG>(smem_u32(drain));
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(drain), 0) && clock64() - t0 < p.wait_limit) {
       }
@@ -964,7 +1124,7 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
         Work w = work0;
         Seg sg{};
         w.next(p, sg);
-        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile);
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
         const float alpha = *alpha_s;
         const int units = min(t.cols, C::BN) * 32;  // float4 groups of the valid columns
         const int u0 = rank * units / p.splits, u1 = (rank + 1) * units / p.splits;
@@ -1014,10 +1174,13 @@ __global__ void __launch_bounds__(320, C::MIN_BLOCKS)
     }
   }
 
+  // A pair's CTAs stay until both are done: the first CTA's MMAs read the second's shared memory
+  // and write its tensor memory, and the second arrives on the first's barriers.
+  if constexpr (C::PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
+    tmem_dealloc<C::CG>(tmem, C::TMEM_COLS);
   }
 }
 

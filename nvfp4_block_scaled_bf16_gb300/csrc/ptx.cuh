@@ -53,6 +53,36 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
+// Arrive on a barrier of another CTA of the cluster (a shared::cluster address from mapa) with
+// the default semantics (release at CTA scope), the form pipelines of CTA pairs use for their
+// hand-offs.  The callers complete what the arrival announces before issuing it (tcgen05.wait::st
+// for tensor-memory writes, tcgen05.wait::ld for reads).  A release at cluster scope was measured
+// at 1000-1500 cycles per arrive (a round trip to L2), against ~40 for this form.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+// Waits that collect arrivals from the other CTA of a pair acquire at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait_sleep_cl(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after `limit` SM clock cycles (or as soon as another role of the
 // CTA has given up), records the time-out in the device status word and returns false.
 struct WaitCtl {
@@ -64,11 +94,14 @@ struct WaitCtl {
 // at least this often.
 constexpr uint32_t kWaitSleepNs = 200000;
 // Bounded wait; on expiry sets bit 0 of the status word and bit 8 + site (which wait gave up).
+// CLUSTER: acquire at cluster scope (the barrier collects arrivals from the peer CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl &w, int site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (CLUSTER ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (CLUSTER ? mbar_try_wait_sleep_cl(bar, parity, kWaitSleepNs) : mbar_try_wait_sleep(bar, parity, kWaitSleepNs))
+      return true;
     if (*w.abort) return false;
     if (clock64() - t0 > w.limit) {
       *w.abort = 1;
@@ -151,17 +184,31 @@ __device__ __forceinline__ void pdl_trigger() {
 }
 
 // ---------------------------------------------------------------- tcgen05
+// CG = 1: one CTA; CG = 2: a CTA pair (cta_group::2), where one warp of EACH of the two CTAs
+// executes the allocation and the deallocation together, and every tcgen05 instruction of the
+// kernel that takes a CTA group uses the same one.
+template <int CG = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
 }
+template <int CG = 1>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
+template <int CG = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -170,9 +217,18 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has completed.
+template <int CG = 1>
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
+  if constexpr (CG == 2)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Pair form: arrive on the barrier at the same shared-memory offset in every CTA of `mask`.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
                : "memory");
 }
 // Registers -> tensor memory: thread i of the warp writes N consecutive 32-bit columns of lane
@@ -215,14 +271,25 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   return v;
 }
 // D (+)= A * B^T with NVFP4 operands: e2m1 data, one ue4m3 scale per 16 K-elements.
+// CG = 2: issued by the pair's first CTA; A's rows and B's rows are split between the two CTAs'
+// shared memory at the same offsets, D and the scales sit at the same TMEM address in each.
+template <int CG = 1>
 __device__ __forceinline__ void mma_nvf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-      " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-      : "memory");
+  if constexpr (CG == 2)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
 }
 // D (+)= A * B^T with MXFP4 operands: e2m1 data, one ue8m0 scale per 32 K-elements.
 __device__ __forceinline__ void mma_mxf4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

@@ -62,9 +62,12 @@ def test_plan_selector_buckets(lib):
     assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
     big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
-    # 512 tiles of 128x256, walked whole and persistently
-    assert big["swap_ab"] == 0 and big["tile_n"] == 256 and big["ctas"] == 152
-    assert big["dp_tiles"] == 512 and big["sk_tiles"] == 0
+    # 256 tiles of 256x256, walked whole and persistently by 76 CTA pairs
+    assert big["swap_ab"] == 0 and big["tile_m"] == 256 and big["tile_n"] == 256 and big["ctas"] == 152
+    assert big["dp_tiles"] == 256 and big["sk_tiles"] == 0 and big["stages"] == 6
+    ragged = lib.nvfp4_gemm_plan(300, 13056, 512)           # 3 x 51 single tiles -> 2 x 51 pair tiles
+    assert ragged["tile_m"] == 256 and ragged["dp_tiles"] == 102 and ragged["ctas"] == 152
+    assert lib.nvfp4_gemm_plan(1024, 4096, 7168)["tile_m"] == 128   # 128 tiles: 128 x 128, single CTAs
     small = lib.nvfp4_gemm_plan(32, 1024, 1024)            # 8 tiles x 4 stages: one stage per CTA
     assert small["splits"] == 4 and small["ctas"] == 32
     few = lib.nvfp4_gemm_plan(640, 1024, 2048)             # 40 tiles but only 2 stages per SM
@@ -77,7 +80,7 @@ def test_plan_selector_buckets(lib):
         if p["swap_ab"]:   # weight rows in 128-row tiles x token columns in tile_n tiles
             tiles = 32 * -(-m // p["tile_n"])
         else:
-            tiles = -(-m // 128) * (4096 // p["tile_n"])
+            tiles = -(-m // p["tile_m"]) * (4096 // p["tile_n"])
         assert p["dp_tiles"] + p["sk_tiles"] == tiles
 
 

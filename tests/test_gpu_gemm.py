@@ -65,6 +65,20 @@ def test_stream_k_splits(nv, m, n, k):
     assert_within(d, R, tol, f"stream-K {m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k", [
+    (300, 13056, 512),    # 2 row tiles: the second CTA of each last-row pair is past M (stores nothing)
+    (520, 9984, 544),     # 8 valid rows in the last pair tile, K tail of 32 (a short last stage)
+    (2304, 4096, 1024)])  # 144 tiles over 76 pairs: accumulators handed back across CTAs
+def test_cta_pair_tiles(nv, m, n, k):
+    """256 x 256 tiles computed by CTA pairs (cta_group::2): every output element checked."""
+    p = nv.nvfp4_gemm_plan(m, n, k)
+    assert p["tile_m"] == 256 and p["tile_n"] == 256 and p["ctas"] % 2 == 0
+    ops = nvfp4_operands(m, n, k, seed=m + k)
+    d = _run(nv, ops)
+    R, tol = reference(ops)
+    assert_within(d, R, tol, f"pair {m}x{n}x{k}")
+
+
 def test_workspace_contract(nv):
     """An explicit workspace works, comes back all zero, gives bit-identical output on reuse;
     a short or missing workspace is refused before anything is launched."""
