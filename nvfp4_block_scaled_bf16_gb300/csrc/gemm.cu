@@ -64,11 +64,13 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     pl.n_tiles = static_cast<int>(ceil_div(m, pl.bn));
     const int tiles = pl.m_tiles * pl.n_tiles;
     // CTA slots to fill: 32-wide tiles run two CTAs per SM, so they split K until both slots of
-    // every SM are taken (at N=4096, K=7168: 8 splits of 3-4 stages, which fit the ring at once,
-    // against 4 splits of 7; 3.5 % faster in a cold PDL chain of decode GEMMs, 10-14 % at larger N)
+    // every SM are taken, at most 7 ways (at N=4096, K=7168: 7 splits of 4 stages, which fit the
+    // ring at once, against 4 splits of 7 stages: 4.5 % faster in a cold PDL chain of decode
+    // GEMMs, 10-14 % at larger N; clusters of 8 launch measurably slower than clusters of 7)
     const int slots = pl.bn == 32 ? 2 * sm_count : sm_count;
     int s = slots / (tiles > 0 ? tiles : 1);
     s = s < 1 ? 1 : (s > 8 ? 8 : s);
+    if (pl.bn == 32 && s > 7) s = 7;
     if (s > pl.k_tiles) s = pl.k_tiles;
     pl.splits = s;
     pl.dp_tiles = tiles;

@@ -272,46 +272,69 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
     const __nv_bfloat16 *xrow = x + (row_ok ? r : 0) * ldx;
     uint8_t *qrow = q + (row_ok ? r : 0) * (static_cast<int64_t>(kb) * 8);
     uint8_t *sf_tile_row = sf + (srow >> 7) * (static_cast<int64_t>(cp) >> 2) * 512 + (srow & 31) * 16 + ((srow >> 5) & 3) * 4;
-    for (int j0 = 0; j0 < cp; j0 += 32) {  // every lane runs the same passes (shuffles below)
-      const int j = j0 + lane;
-      uint32_t code = 0;
-      if (row_ok && j < kb) {
-        float f[16];
-        const uint4 *src = reinterpret_cast<const uint4 *>(xrow + j * 16);
-        bf16x8_to_f32_moe(__ldg(src), f);
-        bf16x8_to_f32_moe(__ldg(src + 1), f + 8);
-        if (SILU) {
-          float u[16];
-          const uint4 *up = reinterpret_cast<const uint4 *>(xrow + up_off + j * 16);
-          bf16x8_to_f32_moe(__ldg(up), u);
-          bf16x8_to_f32_moe(__ldg(up + 1), u + 8);
+    // Passes of 32 blocks, P at a time: all P passes' loads are issued before any is converted,
+    // so a warp keeps P KB in flight instead of one (65.5 -> 52.5 us at T=32768, K=2048).  The
+    // SiLU form is bound by its arithmetic: it keeps one pass, and its registers, for occupancy.
+    constexpr int P = SILU ? 1 : 4;
+    for (int j00 = 0; j00 < cp; j00 += 32 * P) {  // every lane runs the same passes (shuffles below)
+      uint4 xg[P][2], xu[P][2];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+      for (int pp = 0; pp < P; ++pp) {
+        const int j = j00 + 32 * pp + lane;
+        xg[pp][0] = xg[pp][1] = xu[pp][0] = xu[pp][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok && j < kb) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(xrow + j * 16);
+          xg[pp][0] = __ldg(src);
+          xg[pp][1] = __ldg(src + 1);
+          if (SILU) {
+            const uint4 *up = reinterpret_cast<const uint4 *>(xrow + up_off + j * 16);
+            xu[pp][0] = __ldg(up);
+            xu[pp][1] = __ldg(up + 1);
+          }
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
-        code = e4m3_code(sc);
-        const float sd = e4m3_value(code);
-        const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
-        float y0[8], y1[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          y0[i] = __fmul_rn(f[i], inv);
-          y1[i] = __fmul_rn(f[8 + i], inv);
-        }
-        uint2 out;
-        out.x = e2m1x8(y0);
-        out.y = e2m1x8(y1);
-        *reinterpret_cast<uint2 *>(qrow + j * 8) = out;
       }
-      // 4 lanes (scale columns 4c .. 4c+3 of the row) -> one 32-bit word of the 128x4 layout
-      const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
-      const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
-      const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
-      if ((j & 3) == 0 && j < cp)
-        *reinterpret_cast<uint32_t *>(sf_tile_row + (j >> 2) * 512) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+#pragma unroll
+      for (int pp = 0; pp < P; ++pp) {
+        const int j0 = j00 + 32 * pp;
+        if (j0 >= cp) break;  // uniform over the warp
+        const int j = j0 + lane;
+        uint32_t code = 0;
+        if (row_ok && j < kb) {
+          float f[16];
+          bf16x8_to_f32_moe(xg[pp][0], f);
+          bf16x8_to_f32_moe(xg[pp][1], f + 8);
+          if (SILU) {
+            float u[16];
+            bf16x8_to_f32_moe(xu[pp][0], u);
+            bf16x8_to_f32_moe(xu[pp][1], u + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+          }
+          float amax = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+          const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
+          code = e4m3_code(sc);
+          const float sd = e4m3_value(code);
+          const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
+          float y0[8], y1[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            y0[i] = __fmul_rn(f[i], inv);
+            y1[i] = __fmul_rn(f[8 + i], inv);
+          }
+          uint2 out;
+          out.x = e2m1x8(y0);
+          out.y = e2m1x8(y1);
+          *reinterpret_cast<uint2 *>(qrow + j * 8) = out;
+        }
+        // 4 lanes (scale columns 4c .. 4c+3 of the row) -> one 32-bit word of the 128x4 layout
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+        if ((j & 3) == 0 && j < cp)
+          *reinterpret_cast<uint32_t *>(sf_tile_row + (j >> 2) * 512) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+      }
     }
   }
 }

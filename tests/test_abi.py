@@ -56,9 +56,9 @@ def test_plan_selector_buckets(lib):
     """Without a device the selector plans for 152 SMs."""
     for m in (1, 4, 8, 16):
         p = lib.nvfp4_gemm_plan(m, 4096, 7168)
-        # 32 weight tiles, K split 8 ways inside clusters (two CTAs per SM): 256 CTAs
-        assert p["swap_ab"] == 1 and p["tile_n"] == 32 and p["splits"] == 8
-        assert p["dp_tiles"] == 32 and p["sk_tiles"] == 0 and p["ctas"] == 256
+        # 32 weight tiles, K split 7 ways inside clusters (two CTAs per SM): 224 CTAs
+        assert p["swap_ab"] == 1 and p["tile_n"] == 32 and p["splits"] == 7
+        assert p["dp_tiles"] == 32 and p["sk_tiles"] == 0 and p["ctas"] == 224
     assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
     big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
