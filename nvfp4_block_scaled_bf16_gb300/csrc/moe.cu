@@ -194,27 +194,61 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4 *__restric
 // step rounded to nearest even and nothing fused (so it is reproducible off the GPU):
 //   n = rint(t * log2 e); r = (t - n*LN2_HI) - n*LN2_LO; p = Horner(1/k!, k = 7..0); exp = p*2^n
 // with LN2_HI = 0.693145751953125 (16 significant bits, so n*LN2_HI is exact), t > 88 -> inf,
-// t < -87 -> 0.  Within 1.2 fp32 ulps of exp on [-87, 88].
-__device__ __forceinline__ float exp_cw(float t) {
-  if (t > 88.0f) return __int_as_float(0x7F800000);
-  if (t < -87.0f) return 0.0f;
-  const float n = __int2float_rn(__float2int_rn(__fmul_rn(t, 1.44269502162933349609375f)));
-  const float r = __fsub_rn(__fsub_rn(t, __fmul_rn(n, 0.693145751953125f)), __fmul_rn(n, 1.428606765330187045037746429443359375e-06f));
-  float p = 1.98412701138295233249664306640625e-04f;  // 1/7!
-  p = __fadd_rn(__fmul_rn(r, p), 1.388888922519981861114501953125e-03f);  // 1/6!
-  p = __fadd_rn(__fmul_rn(r, p), 8.333333767950534820556640625e-03f);      // 1/5!
-  p = __fadd_rn(__fmul_rn(r, p), 4.16666679084300994873046875e-02f);       // 1/4!
-  p = __fadd_rn(__fmul_rn(r, p), 0.16666667163372039794921875f);          // 1/3!
-  p = __fadd_rn(__fmul_rn(r, p), 0.5f);
-  p = __fadd_rn(__fmul_rn(r, p), 1.0f);
-  p = __fadd_rn(__fmul_rn(r, p), 1.0f);
-  return __fmul_rn(p, __int_as_float((__float2int_rn(n) + 127) << 23));
+// t < -87 -> 0.  Within 1.2 fp32 ulps of exp on [-87, 88].  silu(g) = g * (1 / (1 + exp(-g))).
+// Both run on two values at once with Blackwell's packed fp32 instructions (mul/add/sub
+// .rn.f32x2 round each lane to nearest even exactly as the scalar forms, so each lane's result
+// is that of the scalar steps); the range tests are per-lane selects after the polynomial.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
 }
-
-// h = bf16(silu(g) * u), silu(g) = g * (1 / (1 + exp(-g))), returned as the fp32 value of h.
-__device__ __forceinline__ float silu_mul_bf16(float g, float u) {
-  const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, exp_cw(-g)));
-  return __bfloat162float(__float2bfloat16_rn(__fmul_rn(__fmul_rn(g, sig), u)));
+__device__ __forceinline__ void upk2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t exp_cw2(float t0, float t1) {
+  const uint64_t t = pk2(t0, t1);
+  float m0, m1;
+  upk2(mul2(t, pk2(1.44269502162933349609375f, 1.44269502162933349609375f)), m0, m1);
+  const int i0 = __float2int_rn(m0), i1 = __float2int_rn(m1);
+  const uint64_t n = pk2(__int2float_rn(i0), __int2float_rn(i1));
+  const uint64_t r = sub2(sub2(t, mul2(n, pk2(0.693145751953125f, 0.693145751953125f))),
+                          mul2(n, pk2(1.428606765330187045037746429443359375e-06f, 1.428606765330187045037746429443359375e-06f)));
+  const float c[7] = {1.388888922519981861114501953125e-03f, 8.333333767950534820556640625e-03f,
+                      4.16666679084300994873046875e-02f, 0.16666667163372039794921875f, 0.5f, 1.0f, 1.0f};
+  uint64_t p = pk2(1.98412701138295233249664306640625e-04f, 1.98412701138295233249664306640625e-04f);
+#pragma unroll
+  for (int q = 0; q < 7; ++q) p = add2(mul2(r, p), pk2(c[q], c[q]));
+  float e0, e1;
+  upk2(mul2(p, pk2(__int_as_float((i0 + 127) << 23), __int_as_float((i1 + 127) << 23))), e0, e1);
+  e0 = t0 > 88.0f ? __int_as_float(0x7F800000) : (t0 < -87.0f ? 0.0f : e0);
+  e1 = t1 > 88.0f ? __int_as_float(0x7F800000) : (t1 < -87.0f ? 0.0f : e1);
+  return pk2(e0, e1);
+}
+// (g0, g1), (u0, u1) -> the fp32 values of h = bf16(silu(g) * u) for both
+__device__ __forceinline__ void silu_mul_bf16x2(float &g0, float &g1, float u0, float u1) {
+  float d0, d1;
+  upk2(add2(pk2(1.0f, 1.0f), exp_cw2(-g0, -g1)), d0, d1);
+  const uint64_t sig = pk2(__fdiv_rn(1.0f, d0), __fdiv_rn(1.0f, d1));
+  float h0, h1;
+  upk2(mul2(mul2(pk2(g0, g1), sig), pk2(u0, u1)), h0, h1);
+  g0 = __bfloat162float(__float2bfloat16_rn(h0));
+  g1 = __bfloat162float(__float2bfloat16_rn(h1));
 }
 
 __device__ __forceinline__ void bf16x8_to_f32_moe(const uint4 &v, float *f) {
@@ -308,7 +342,7 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
             bf16x8_to_f32_moe(xu[pp][0], u);
             bf16x8_to_f32_moe(xu[pp][1], u + 8);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = silu_mul_bf16(f[i], u[i]);
+            for (int i = 0; i < 8; ++i) silu_mul_bf16x2(f[2 * i], f[2 * i + 1], u[2 * i], u[2 * i + 1]);
           }
           float amax = 0.0f;
 #pragma unroll
