@@ -178,6 +178,28 @@ nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b
                           void *workspace, size_t workspace_bytes, uint32_t flags,
                           nvfp4_stream_t stream);
 
+/* nvfp4_quantize fused into nvfp4_gemm: D = nvfp4_gemm(nvfp4_quantize(x, gs_x), b), with the
+ * activation quantised inside the GEMM kernel, so its codes and scales never go through global
+ * memory and one launch replaces two.  Not an operation of the pages; it is the "quantise in
+ * the GEMM's prologue" extension of [vLLM-SM103] "add pdl" (the PDL edge between the two).
+ * The result is bit-identical to the two calls: every 16-element block is quantised with the
+ * same arithmetic as nvfp4_quantize and the MMAs consume it in the same order.
+ *   x      bf16 [m, k] row-major, row stride ldx >= k elements, 16-B aligned, ldx % 8 == 0
+ *   gs_x   device fp32 scalar: x's global scale, as nvfp4_quantize's
+ *   b, sfb, alpha, d, workspace, flags, stream: as nvfp4_gemm (NVFP4_FLAG_SF_SM103: sfb is in
+ *          the SM103 layout); these plans split K inside clusters and need no workspace.
+ *   1 <= m <= 256 (the weight-streaming plans, where each CTA quantises the token rows it
+ *   needs); larger m: NVFP4_ERR_UNSUPPORTED_SHAPE, nothing launched (quantise separately).
+ *   Every CTA that shares a token tile quantises it again (once per 128 weight rows), so the
+ *   fused call is faster than the PDL-chained pair only for a few tokens (measured on GB300,
+ *   N=4096, K=7168, cold weights: M=1 3 % faster, M=4 even, M >= 16 slower).
+ * With NVFP4_FLAG_PDL, b and sfb may be read before the wait for the preceding kernel; x after it.
+ */
+nvfp4_status_t nvfp4_quantize_gemm(const void *x, int64_t ldx, const float *gs_x, const uint8_t *b,
+                                   const uint8_t *sfb, const float *alpha, void *d, int64_t m, int64_t n,
+                                   int64_t k, void *workspace, size_t workspace_bytes, uint32_t flags,
+                                   nvfp4_stream_t stream);
+
 /* nvfp4_gemm without a workspace argument: when the plan splits tiles stream-K, the partial
  * tiles and arrival counters go to a static 20 MiB device array inside the library instead of a
  * caller buffer.  The pages have no counterpart of this entry point: it exists for callers that

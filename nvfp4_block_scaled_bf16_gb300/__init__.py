@@ -45,6 +45,7 @@ _SIGS = {
     "nvfp4_gemm_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(_sz)]),
     "nvfp4_gemm": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     "nvfp4_gemm_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
+    "nvfp4_quantize_gemm": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     "mxfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "sf_swizzle": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
     "nvfp4_sf_convert_layout": (_int, [_vp, _vp, _i64, _i64, _int, _vp]),
@@ -207,6 +208,31 @@ def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None, works
     _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
                            _ptr(workspace), 0 if workspace is None else workspace.numel(), flags,
                            _stream(stream)))
+    return d
+
+
+def nvfp4_quantize_gemm(x, gs, b, sfb, alpha, d=None, flags: int = 0, stream=None):
+    """nvfp4_gemm(*nvfp4_quantize(x, gs), b, sfb, alpha) in one kernel (1 <= m <= 256): x bf16
+    [m, k] with contiguous rows, b [n, k/2] packed uint8; bit-identical to the two calls."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(gs, torch.float32, "gs")
+    _need(b, torch.uint8, "b", 2)
+    _need(sfb, torch.uint8, "sfb")
+    _need(alpha, torch.float32, "alpha")
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    if not b.is_contiguous():
+        raise ValueError("b must be contiguous")
+    m, k = x.shape
+    n = b.shape[0]
+    if b.shape[1] * 2 != k:
+        raise ValueError("x and b disagree on K")
+    if sfb.numel() < sf_bytes(n, k):
+        raise ValueError("sfb is too small")
+    if d is None:
+        d = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _check(_lib.nvfp4_quantize_gemm(_ptr(x), x.stride(0), _ptr(gs), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, k,
+                                    None, 0, flags, _stream(stream)))
     return d
 
 

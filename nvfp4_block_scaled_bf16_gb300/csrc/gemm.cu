@@ -186,33 +186,47 @@ extern "C" nvfp4_status_t nvfp4_gemm_workspace_size(int64_t m, int64_t n, int64_
   return NVFP4_OK;
 }
 
-extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b,
-                                     const uint8_t *sfb, const float *alpha, void *d, int64_t m,
-                                     int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
-                                     uint32_t flags, nvfp4_stream_t stream) {
-  clear_error();
+namespace nvfp4 {
+namespace {
+
+// Activation to quantise inside the kernel (nvfp4_quantize_gemm); a == nullptr: none.
+struct FusedA {
+  const __nv_bfloat16 *x;
+  int64_t ldx;
+  const float *gs;
+};
+
+nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb,
+                        const float *alpha, void *d, int64_t m, int64_t n, int64_t k, void *workspace,
+                        size_t workspace_bytes, uint32_t flags, nvfp4_stream_t stream, const FusedA &fq) {
+  const bool fused = fq.x != nullptr;
   if (m < 0 || n <= 0 || k <= 0 || m >= (1LL << 31) || n >= (1LL << 31) || k >= (1LL << 31))
-    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: m=%lld n=%lld k=%lld", (long long)m, (long long)n, (long long)k);
+    return fail(NVFP4_ERR_INVALID_ARG, "%s: m=%lld n=%lld k=%lld", name, (long long)m, (long long)n, (long long)k);
   if (k % 32 || n % 32)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "nvfp4_gemm: need k %% 32 == 0 and n %% 32 == 0 (k=%lld n=%lld)", (long long)k, (long long)n);
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: need k %% 32 == 0 and n %% 32 == 0 (k=%lld n=%lld)", name, (long long)k, (long long)n);
   if (flags & ~(uint32_t)(NVFP4_FLAG_PDL | NVFP4_FLAG_DEBUG_TIMEOUT | NVFP4_FLAG_DEBUG_SKIP_FIRST_LOAD | NVFP4_FLAG_SF_SM103))
-    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: unknown flags 0x%x", flags);
+    return fail(NVFP4_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
   if (m == 0) return NVFP4_OK;
-  if (!a || !sfa || !b || !sfb || !alpha || !d) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: null pointer");
-  if (!aligned(a, 32) || !aligned(b, 32) || !aligned(d, 32) || !aligned(sfa, 16) || !aligned(sfb, 16) || !aligned(alpha, 4))
-    return fail(NVFP4_ERR_MISALIGNED, "nvfp4_gemm: a, b, d need 32-B and sfa, sfb 16-B alignment");
+  if ((!fused && (!a || !sfa)) || !b || !sfb || !alpha || !d) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", name);
+  if ((!fused && (!aligned(a, 32) || !aligned(sfa, 16))) || !aligned(b, 32) || !aligned(d, 32) || !aligned(sfb, 16) ||
+      !aligned(alpha, 4))
+    return fail(NVFP4_ERR_MISALIGNED, "%s: a, b, d need 32-B and sfa, sfb 16-B alignment", name);
   DeviceInfo dev;
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
 
   const Plan pl = select_plan(m, n, k, dev.sm_count);
+  if (fused && !pl.swap)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "%s: the quantisation is fused into the weight-streaming plans (m <= 256, got %lld); quantise with "
+                "nvfp4_quantize and call nvfp4_gemm", name, (long long)m);
   st = with_config(pl, [&](auto cfg) { return prepare<decltype(cfg)>(dev); });
   if (st != NVFP4_OK) return st;
   if (pl.ws_bytes > 0) {
     if (!workspace || workspace_bytes < pl.ws_bytes)
-      return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gemm: this shape needs a workspace of %zu bytes (got %zu%s)",
+      return fail(NVFP4_ERR_INVALID_ARG, "%s: this shape needs a workspace of %zu bytes (got %zu%s)", name,
                   pl.ws_bytes, workspace_bytes, workspace ? "" : ", NULL");
-    if (!aligned(workspace, kWsAlign)) return fail(NVFP4_ERR_MISALIGNED, "nvfp4_gemm: workspace needs 256-B alignment");
+    if (!aligned(workspace, kWsAlign)) return fail(NVFP4_ERR_MISALIGNED, "%s: workspace needs 256-B alignment", name);
   }
   // Kernel operand A fills the 128-row MMA slot; with swap it is the weight B.
   const uint8_t *opa = pl.swap ? b : a, *opb = pl.swap ? a : b;
@@ -221,9 +235,13 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   CUtensorMap ta, tb, tb3;
   st = encode_tmap_2d_u8(&ta, opa, k / 2, rows_a, k / 2, 128, 128, true);
   if (st != NVFP4_OK) return st;
-  st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.pair ? pl.bn / 2 : pl.bn, true);
-  if (st != NVFP4_OK) return st;
-  if (pl.resident) {
+  if (fused) {
+    tb = ta;  // operand B is produced in the kernel: its maps are unused
+  } else {
+    st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.pair ? pl.bn / 2 : pl.bn, true);
+    if (st != NVFP4_OK) return st;
+  }
+  if (pl.resident && !fused) {
     st = encode_tmap_stages_u8(&tb3, opb, k / 2, rows_b, pl.bn, pl.nst_max);
     if (st != NVFP4_OK) return st;
   } else {
@@ -232,7 +250,7 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
 
   GemmArgs args{};
   args.sfa = sfopa;
-  args.sfb = sfopb;
+  args.sfb = fused ? sfopa : sfopb;  // (unused when fused)
   args.alpha = alpha;
   args.d = static_cast<__nv_bfloat16 *>(d);
   args.ldd = n;
@@ -256,6 +274,9 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
   args.nst_max = pl.nst_max;
   args.lookahead = pl.lookahead;
   args.sf_sm103 = (flags & NVFP4_FLAG_SF_SM103) ? 1 : 0;
+  args.xq = fq.x;
+  args.ldx = fq.ldx;
+  args.gs_q = fq.gs;
   if (pl.sk_tiles > 0) {
     args.ws_cnt = static_cast<unsigned int *>(workspace);
     args.ws = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
@@ -267,6 +288,32 @@ extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const
     using C = decltype(cfg);
     const cudaError_t e = launch(bs_gemm_kernel<C, false>, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
                                  (flags & NVFP4_FLAG_PDL) != 0, pl.pair ? 2 : pl.splits, ta, tb, tb3, args);
-    return check_launch(e, "nvfp4_gemm");
+    return check_launch(e, name);
   });
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b,
+                                     const uint8_t *sfb, const float *alpha, void *d, int64_t m,
+                                     int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
+                                     uint32_t flags, nvfp4_stream_t stream) {
+  clear_error();
+  return run_gemm("nvfp4_gemm", a, sfa, b, sfb, alpha, d, m, n, k, workspace, workspace_bytes, flags, stream,
+                  FusedA{nullptr, 0, nullptr});
+}
+
+extern "C" nvfp4_status_t nvfp4_quantize_gemm(const void *x, int64_t ldx, const float *gs_x, const uint8_t *b,
+                                              const uint8_t *sfb, const float *alpha, void *d, int64_t m,
+                                              int64_t n, int64_t k, void *workspace, size_t workspace_bytes,
+                                              uint32_t flags, nvfp4_stream_t stream) {
+  clear_error();
+  if (m > 0 && (!x || !gs_x)) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_gemm: null pointer");
+  if (m > 0 && ldx < k)
+    return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_quantize_gemm: ldx=%lld < k=%lld", (long long)ldx, (long long)k);
+  if (m > 0 && (!aligned(x, 16) || ldx % 8 || !aligned(gs_x, 4)))
+    return fail(NVFP4_ERR_MISALIGNED, "nvfp4_quantize_gemm: x needs 16-B alignment and ldx %% 8 == 0");
+  return run_gemm("nvfp4_quantize_gemm", nullptr, nullptr, b, sfb, alpha, d, m, n, k, workspace, workspace_bytes,
+                  flags, stream, FusedA{static_cast<const __nv_bfloat16 *>(x), ldx, gs_x});
 }

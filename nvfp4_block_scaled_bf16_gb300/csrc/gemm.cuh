@@ -181,6 +181,12 @@ struct GemmArgs {
                               // issued once stage i has landed); 0: as many as the ring holds
   int sf_sm103;               // 1: both scale buffers are in the SM103 layout
   int alpha_per_expert;       // grouped: alpha points to one fp32 per expert
+  // Fused quantisation (swap-AB plans only; xq == nullptr: off): operand B is the bf16
+  // activation xq [n, k] (row stride ldx elements) under global scale *gs_q, quantised to NVFP4
+  // inside the kernel instead of loaded; sfb is then unused.
+  const __nv_bfloat16 *xq;
+  int64_t ldx;
+  const float *gs_q;
 };
 
 // The 16 scale bytes of 512-byte scale tile `tile` that lane i of a scale writer puts in its
@@ -369,7 +375,7 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
       bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES),
                 t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
   }
-  if (do_b) {
+  if (do_b && !(C::SWAP_ONLY && p.xq)) {
     tma_load_2d(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt * 128, t.b_y);
     if constexpr (!C::PAIR)
       for (int b = 0; b < t.sfb_blocks; ++b)
@@ -382,6 +388,7 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
 template <class C>
 __device__ __forceinline__ uint32_t stage_tx(const GemmArgs &p, const TileInfo &t, int kt) {
   if constexpr (C::PAIR) return C::A_BYTES + C::B_BYTES;
+  else if (C::SWAP_ONLY && p.xq) return C::A_BYTES + stage_chunks<C>(p, kt) * 512;  // B is quantised in-kernel
   else return C::A_BYTES + C::B_BYTES + stage_chunks<C>(p, kt) * 512 * (1 + t.sfb_blocks);
 }
 
@@ -463,6 +470,104 @@ __device__ __forceinline__ void sk_fixup(const GemmArgs &p, const TileInfo &t, c
   }
 }
 
+// Fused quantisation (swap-AB plans): the four epilogue warps, idle until the accumulator is
+// ready, quantise the activation rows of the CTA's K stages into the stages' operand-B tiles
+// (e2m1 codes in the 128-byte swizzle the TMA would have produced) and B-scale chunks (e4m3,
+// 128x4 or SM103 layout), block by block with the standalone quantiser's arithmetic
+// (nvfp4_block16), so the MMAs see exactly the operand nvfp4_quantize would have written.  Rows
+// without a token and K positions past k are zero, as the TMA's out-of-bounds fill.  Each
+// thread keeps 4 blocks' loads in flight; then the writes are fenced for the tensor cores and
+// one thread makes the second arrival on the stage's full barrier (resident slices: on every
+// stage's barrier once all are written, because the scale writers take all stages' scales after
+// stage 0 lands).  Every CTA of a token tile quantises that tile's slice again, once per weight
+// tile, so this pays only for a few tokens.  Returns false when a wait gave up.
+template <class C, bool GROUPED>
+__device__ __forceinline__ void quantize_b_block(const GemmArgs &p, const TileInfo &t, uint8_t *smem, int stage, int kt,
+                                                 int r, int b, const uint4 &lo, const uint4 &hi, float gs) {
+  uint32_t code = 0;
+  uint2 out = make_uint2(0u, 0u);
+  if (kt * 256 + b * 16 < p.k) {
+    float f[16];
+    bf16x16_to_f32(lo, hi, f);
+    out = nvfp4_block16(f, gs, code);
+  }
+  *reinterpret_cast<uint2 *>(smem + C::B_REGION + stage * C::B_BYTES + r * 128 + (((b >> 1) ^ (r & 7)) << 4) +
+                             (b & 1) * 8) = out;
+  const int m = r & 127;
+  const int in_tile = p.sf_sm103 ? ((m >> 4) & 7) * 16 + ((m >> 2) & 3) * 128 + (m & 3) * 4 + (b & 3)
+                                 : (m & 31) * 16 + (m >> 5) * 4 + (b & 3);
+  smem[C::SFB_REGION + stage * C::SFB_BYTES + ((r >> 7) * C::CHUNKS + (b >> 2)) * 512 + in_tile] =
+      static_cast<uint8_t>(code);
+}
+
+template <class C, bool GROUPED>
+__device__ bool quantize_operand_b(const GemmArgs &p, const Tables<C, GROUPED> &tb, Work w, int crank, uint8_t *smem,
+                                   uint64_t *full, uint64_t *empty, const WaitCtl &wc, int tid) {
+  Seg sg;
+  if (!w.next(p, sg)) return true;  // (swap-AB CTAs hold one segment)
+  const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
+  const float gs = __ldg(p.gs_q);
+  const int rows = t.cols < C::BN ? t.cols : C::BN;  // tokens in this tile (operand B rows)
+  // Rows without a token, and the scale rows nobody fills, are zero in every stage slot; they
+  // are written once here (the slots are reused, the tile's token count is fixed).
+  for (int i = tid; i < C::STAGES * C::SFB_BYTES / 16; i += 128)
+    *reinterpret_cast<uint4 *>(smem + C::SFB_REGION + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
+  const int pad16 = (C::BN - rows) * 8;  // 16-byte words of padding rows per stage slot
+  for (int i = tid; i < C::STAGES * pad16; i += 128) {
+    const int st = i / pad16, o = i - st * pad16;
+    *reinterpret_cast<uint4 *>(smem + C::B_REGION + st * C::B_BYTES + rows * 128 + 16 * o) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const bool resident = p.resident != 0;
+  const int nst = sg.kt1 - sg.kt0;
+  // Blocks with data: (stage, token row, 16-element block); a resident slice takes all its
+  // stages at once, the ring one stage at a time.  Each thread keeps QB blocks' loads in flight.
+  constexpr int QB = 4;
+  const int per_stage = rows * 16;
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int s0 = 0; s0 < nst;) {
+    const int s1 = resident ? nst : s0 + 1;  // stages [s0, s1) of this pass
+    if (!resident && !mbar_wait(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) return false;
+    const int total = (s1 - s0) * per_stage;
+    for (int base = tid; base < total; base += 128 * QB) {
+      uint4 lo[QB], hi[QB];
+#pragma unroll
+      for (int u = 0; u < QB; ++u) {
+        const int idx = base + 128 * u;
+        lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < total) {
+          const int ls = idx / per_stage, rem = idx - ls * per_stage;
+          const int r = rem >> 4, b = rem & 15, k0 = (sg.kt0 + s0 + ls) * 256 + b * 16;
+          if (k0 < p.k) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.xq + (t.b_y + r) * p.ldx + k0);
+            lo[u] = __ldg(src);
+            hi[u] = __ldg(src + 1);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < QB; ++u) {
+        const int idx = base + 128 * u;
+        if (idx < total) {
+          const int ls = idx / per_stage, rem = idx - ls * per_stage;
+          quantize_b_block<C, GROUPED>(p, t, smem, resident ? s0 + ls : stage, sg.kt0 + s0 + ls, rem >> 4, rem & 15,
+                                       lo[u], hi[u], gs);
+        }
+      }
+    }
+    fence_proxy_async_smem();  // generic writes -> visible to the tensor cores' reads
+    named_barrier_sync(2, 128);
+    if (tid == 0)
+      for (int i = s0; i < s1; ++i) mbar_arrive(smem_u32(&full[resident ? i : stage]));
+    s0 = s1;
+    if (!resident && ++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
 // Arrive on `bar` once the calling thread's tcgen05 operations so far are complete; for a CTA
 // pair, on the barrier at that offset in both CTAs.
 template <class C>
@@ -500,6 +605,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int crank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // place in the CTA pair
+  const bool fused_q = C::SWAP_ONLY && p.xq != nullptr;  // operand B quantised in-kernel
   const WaitCtl wc{p.wait_limit, abort_flag, p.status};
   // The next kernel may launch now: it waits (griddepcontrol.wait) for this grid to complete
   // before it reads our output, and its CTAs can meanwhile take the SM space we leave free.
@@ -507,7 +613,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), fused_q ? 2 : 1);  // fused: the quantising warps arrive too
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -544,14 +650,15 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         const int mb = tile % p.m_tiles, b_y = (tile / p.m_tiles) * C::BN;
         const uint8_t *sfa_blk = p.sfa + (static_cast<int64_t>(mb) * p.sf_chunks + kt0 * C::CHUNKS) * 512;
         const uint8_t *sfb_blk = p.sfb + (static_cast<int64_t>(b_y / 128) * p.sf_chunks + kt0 * C::CHUNKS) * 512;
-        mbar_arrive_expect_tx(smem_u32(&full[0]), C::A_BYTES + p.nst_max * C::B_BYTES + nst * (C::SFA_BYTES + C::SFB_BYTES));
+        mbar_arrive_expect_tx(smem_u32(&full[0]), fused_q ? C::A_BYTES + nst * C::SFA_BYTES
+                                                          : C::A_BYTES + p.nst_max * C::B_BYTES + nst * (C::SFA_BYTES + C::SFB_BYTES));
         for (int i = 1; i < nst; ++i) mbar_arrive_expect_tx(smem_u32(&full[i]), C::A_BYTES);
         bulk_load(smem_u32(smem + C::SFA_REGION), sfa_blk, nst * C::SFA_BYTES, smem_u32(&full[0]));
         const int first = p.lookahead > 0 && p.lookahead < nst ? p.lookahead : nst;
         for (int i = 0; i < first; ++i)
           if (!(p.debug_skip_first_load && i == 0))
             tma_load_2d(smem_u32(smem + i * C::A_BYTES), &tmA, smem_u32(&full[i]), (kt0 + i) * 128, mb * 128);
-        if (p.weight_operand != 1) {
+        if (p.weight_operand != 1 && !fused_q) {
           tma_load_3d(smem_u32(smem + C::B_REGION), &tmB3, smem_u32(&full[0]), 0, b_y, kt0);
           bulk_load(smem_u32(smem + C::SFB_REGION), sfb_blk, nst * C::SFB_BYTES, smem_u32(&full[0]));
         }
@@ -619,7 +726,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         Seg s0;
         if (Work(work0).next(p, s0)) {
           const TileInfo t = tile_info<C, GROUPED>(p, tb, s0.tile, crank);
-          if (p.weight_operand == 1) {
+          if (p.weight_operand == 1 && !fused_q) {
             pdl_wait();
             tma_load_3d(smem_u32(smem + C::B_REGION), &tmB3, smem_u32(&full[0]), 0, t.b_y, s0.kt0);
             bulk_load(smem_u32(smem + C::SFB_REGION), t.sfb_blk + static_cast<int64_t>(s0.kt0) * C::CHUNKS * 512,
@@ -949,6 +1056,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     const int quad = warp & 3;  // tcgen05.ld: warp w reaches lanes 32*(w%4) .. +31
     const int row = quad * 32 + lane;
     const int tid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
+    if constexpr (C::SWAP_ONLY) {
+      // (a wait that gave up set the abort flag; the epilogue below then does no work)
+      if (fused_q) quantize_operand_b<C, GROUPED>(p, tb, work0, crank, smem, full, empty, wc, tid);
+    }
     // alpha is read by one thread and shared: a load left to each thread's first use was
     // scheduled there, putting a full memory latency (~1400 cycles) in front of the stores.
     if (tid == 0) *alpha_s = p.alpha ? *p.alpha : 1.0f;

@@ -344,23 +344,7 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
 #pragma unroll
             for (int i = 0; i < 8; ++i) silu_mul_bf16x2(f[2 * i], f[2 * i + 1], u[2 * i], u[2 * i + 1]);
           }
-          float amax = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-          const float sc = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
-          code = e4m3_code(sc);
-          const float sd = e4m3_value(code);
-          const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
-          float y0[8], y1[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            y0[i] = __fmul_rn(f[i], inv);
-            y1[i] = __fmul_rn(f[8 + i], inv);
-          }
-          uint2 out;
-          out.x = e2m1x8(y0);
-          out.y = e2m1x8(y1);
-          *reinterpret_cast<uint2 *>(qrow + j * 8) = out;
+          *reinterpret_cast<uint2 *>(qrow + j * 8) = nvfp4_block16(f, gs, code);
         }
         // 4 lanes (scale columns 4c .. 4c+3 of the row) -> one 32-bit word of the 128x4 layout
         const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);

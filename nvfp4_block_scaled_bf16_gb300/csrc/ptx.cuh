@@ -407,6 +407,37 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
   if (e == 0) return __uint2float_rn(m) * 0.001953125f;  // m * 2^-9, exact
   return __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
 }
+// One 16-element NVFP4 block under global scale gs: the e4m3 code of gs * amax / 6 (RNE,
+// saturating) and the 16 e2m1 codes of x * (gs / scale) packed two per byte (element 2t in the
+// low nibble of byte t); a zero scale gives zero codes.  Every quantiser of the library calls
+// this, so a block quantised anywhere gets the same codes.
+__device__ __forceinline__ uint2 nvfp4_block16(const float (&f)[16], float gs, uint32_t &code) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  code = e4m3_code(__fdiv_rn(__fmul_rn(gs, amax), 6.0f));
+  const float sd = e4m3_value(code);
+  const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
+  float y0[8], y1[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    y0[i] = __fmul_rn(f[i], inv);
+    y1[i] = __fmul_rn(f[8 + i], inv);
+  }
+  uint2 out;
+  out.x = e2m1x8(y0);
+  out.y = e2m1x8(y1);
+  return out;
+}
+// Sixteen bf16 (two 16-byte words) -> fp32, element order kept.
+__device__ __forceinline__ void bf16x16_to_f32(const uint4 &a, const uint4 &b, float (&f)[16]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
 // Smallest ue8m0 code with 2^(code-127) >= s (s >= 0), clamped to [0, 254].
 __device__ __forceinline__ uint32_t ue8m0_code_up(float s) {
   const uint32_t b = __float_as_uint(s);

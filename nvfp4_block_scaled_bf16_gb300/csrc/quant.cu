@@ -70,25 +70,8 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *_
     if (r < m && j < kb) {
       const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
       float f[16];
-      bf16x8_to_f32(__ldg(src), f);
-      bf16x8_to_f32(__ldg(src + 1), f + 8);
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      const float s = __fdiv_rn(__fmul_rn(gs, amax), 6.0f);
-      code = e4m3_code(s);
-      const float sd = e4m3_value(code);
-      const float inv = (sd == 0.0f) ? 0.0f : __fdiv_rn(gs, sd);
-      float y0[8], y1[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        y0[i] = __fmul_rn(f[i], inv);
-        y1[i] = __fmul_rn(f[8 + i], inv);
-      }
-      uint2 out;
-      out.x = e2m1x8(y0);
-      out.y = e2m1x8(y1);
-      *reinterpret_cast<uint2 *>(q + r * (kb * 8) + j * 8) = out;
+      bf16x16_to_f32(__ldg(src), __ldg(src + 1), f);
+      *reinterpret_cast<uint2 *>(q + r * (kb * 8) + j * 8) = nvfp4_block16(f, gs, code);
     }
     const uint32_t word = gather4(code);
     if ((j & 3) == 0) *reinterpret_cast<uint32_t *>(sf + (SM103 ? sf_offset_sm103(r, j, cp) : sf_offset(r, j, cp))) = word;

@@ -112,6 +112,20 @@ def test_gemm_rejects_bad_arguments_without_a_device(lib):
     assert L.nvfp4_gemm(None, None, None, None, None, None, 0, 1024, 1024, None, 0, 0, None) == 0
 
 
+def test_fused_quantize_gemm_rejects_bad_arguments_without_a_device(lib):
+    L = lib.lib
+    X, G, B, S, D = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000  # never dereferenced
+    q = L.nvfp4_quantize_gemm
+    assert q(None, 1024, _c(G), _c(B), _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 1   # x
+    assert q(_c(X), 1024, None, _c(B), _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 1   # gs
+    assert q(_c(X), 512, _c(G), _c(B), _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 1   # ldx < k
+    assert q(_c(X + 8), 1024, _c(G), _c(B), _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 2
+    assert q(_c(X), 1028, _c(G), _c(B), _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 2  # ldx % 8
+    assert q(_c(X), 1024, _c(G), _c(B), _c(S), _c(G), _c(D), 8, 1024, 1000, None, 0, 0, None) == 3  # k % 32
+    assert q(_c(X), 1024, _c(G), None, _c(S), _c(G), _c(D), 8, 1024, 1024, None, 0, 0, None) == 1   # b
+    assert q(None, 0, None, None, None, None, None, 0, 1024, 1024, None, 0, 0, None) == 0          # m = 0
+
+
 def test_quantizers_reject_bad_arguments_without_a_device(lib):
     L = lib.lib
     X, G, Q, S = 0x10000, 0x20000, 0x30000, 0x40000
