@@ -154,9 +154,9 @@ nvfp4_status_t with_config(const Plan &pl, F &&f) {
 }
 
 // Raises the kernel's dynamic shared-memory limit (once per kernel and device).
-template <class C>
+template <class C, bool FUSED = false>
 nvfp4_status_t prepare(const DeviceInfo &dev) {
-  return allow_smem(reinterpret_cast<const void *>(bs_gemm_kernel<C, false>), C::smem_bytes(false), dev.device);
+  return allow_smem(reinterpret_cast<const void *>(bs_gemm_kernel<C, false, FUSED>), C::smem_bytes(false), dev.device);
 }
 
 }  // namespace
@@ -220,7 +220,13 @@ nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, 
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "%s: the quantisation is fused into the weight-streaming plans (m <= 256, got %lld); quantise with "
                 "nvfp4_quantize and call nvfp4_gemm", name, (long long)m);
-  st = with_config(pl, [&](auto cfg) { return prepare<decltype(cfg)>(dev); });
+  st = with_config(pl, [&](auto cfg) {
+    using C = decltype(cfg);
+    if constexpr (C::SWAP_ONLY) {
+      if (fused) return prepare<C, true>(dev);
+    }
+    return prepare<C>(dev);
+  });
   if (st != NVFP4_OK) return st;
   if (pl.ws_bytes > 0) {
     if (!workspace || workspace_bytes < pl.ws_bytes)
@@ -286,8 +292,15 @@ nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, 
   cudaStream_t s = (cudaStream_t)stream;
   return with_config(pl, [&](auto cfg) {
     using C = decltype(cfg);
+    const bool pdl = (flags & NVFP4_FLAG_PDL) != 0;
+    const int cx = pl.pair ? 2 : pl.splits;
+    if constexpr (C::SWAP_ONLY) {
+      if (fused)
+        return check_launch(launch(bs_gemm_kernel<C, false, true>, dim3(pl.ctas), dim3(C::THREADS),
+                                   C::smem_bytes(false), s, pdl, cx, ta, tb, tb3, args), name);
+    }
     const cudaError_t e = launch(bs_gemm_kernel<C, false>, dim3(pl.ctas), dim3(C::THREADS), C::smem_bytes(false), s,
-                                 (flags & NVFP4_FLAG_PDL) != 0, pl.pair ? 2 : pl.splits, ta, tb, tb3, args);
+                                 pdl, cx, ta, tb, tb3, args);
     return check_launch(e, name);
   });
 }

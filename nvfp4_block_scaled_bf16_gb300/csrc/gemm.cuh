@@ -363,7 +363,7 @@ __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
 // Copies of K stage kt into ring slot stg (only the requested operand halves), all issued by the
 // calling thread: a copy instruction costs the issuing thread ~100 cycles whatever its size,
 // and spreading them over divergent lanes of one warp was measured slower still.
-template <class C>
+template <class C, bool FUSED = false>
 __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t, int kt, int stg, uint8_t *smem,
                                             uint64_t *full, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                             bool do_a, bool do_b) {
@@ -375,7 +375,7 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
       bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES),
                 t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
   }
-  if (do_b && !(C::SWAP_ONLY && p.xq)) {
+  if (do_b && !FUSED) {
     tma_load_2d(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt * 128, t.b_y);
     if constexpr (!C::PAIR)
       for (int b = 0; b < t.sfb_blocks; ++b)
@@ -385,10 +385,10 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
 }
 
 // Bytes that land on full[] for K stage kt (operands, and scales unless they have their own ring).
-template <class C>
+template <class C, bool FUSED = false>
 __device__ __forceinline__ uint32_t stage_tx(const GemmArgs &p, const TileInfo &t, int kt) {
   if constexpr (C::PAIR) return C::A_BYTES + C::B_BYTES;
-  else if (C::SWAP_ONLY && p.xq) return C::A_BYTES + stage_chunks<C>(p, kt) * 512;  // B is quantised in-kernel
+  else if constexpr (FUSED) return C::A_BYTES + stage_chunks<C>(p, kt) * 512;  // B is quantised in-kernel
   else return C::A_BYTES + C::B_BYTES + stage_chunks<C>(p, kt) * 512 * (1 + t.sfb_blocks);
 }
 
@@ -576,7 +576,9 @@ __device__ __forceinline__ void commit_to(uint32_t bar) {
   else tc_commit(bar);
 }
 
-template <class C, bool GROUPED>
+// FUSED (swap-AB configurations only): operand B is quantised in the kernel (GemmArgs::xq); a
+// separate instantiation, so the other kernels carry none of that code.
+template <class C, bool GROUPED, bool FUSED = false>
 __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmB3, const GemmArgs p) {
@@ -605,7 +607,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int crank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // place in the CTA pair
-  const bool fused_q = C::SWAP_ONLY && p.xq != nullptr;  // operand B quantised in-kernel
+  constexpr bool fused_q = FUSED;  // operand B quantised in-kernel
+  static_assert(!FUSED || (C::SWAP_ONLY && !GROUPED), "fused quantisation serves the swap-AB plans");
   const WaitCtl wc{p.wait_limit, abort_flag, p.status};
   // The next kernel may launch now: it waits (griddepcontrol.wait) for this grid to complete
   // before it reads our output, and its CTAs can meanwhile take the SM space we leave free.
@@ -756,8 +759,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           pre = min(p.lookahead > 0 ? p.lookahead : C::STAGES, min(C::STAGES, s0.kt1 - s0.kt0));
           for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
             const int kt = s0.kt0 + i;
-            mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx<C>(p, t, kt));
-            if (!(skip_first && i == 0)) issue_stage<C>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
+            mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx<C, FUSED>(p, t, kt));
+            if (!(skip_first && i == 0)) issue_stage<C, FUSED>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
           }
           if (C::SWAP_ONLY && pre_a) {
             // The rest of this CTA's weight slice goes to L2 now, while the preceding kernel runs;
@@ -780,11 +783,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
             }
             if (!early_stage) {
               if (!mbar_wait<C::PAIR>(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) goto producer_done;
-              mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx<C>(p, t, kt));
+              mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx<C, FUSED>(p, t, kt));
             }
             const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
             if (!(skip_first && issued == 0) && (do_a || do_b))
-              issue_stage<C>(p, t, kt, stage, smem, full, &tmA, &tmB, do_a, do_b);
+              issue_stage<C, FUSED>(p, t, kt, stage, smem, full, &tmA, &tmB, do_a, do_b);
             ++issued;
             if (++stage == C::STAGES) {
               stage = 0;
@@ -1056,9 +1059,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     const int quad = warp & 3;  // tcgen05.ld: warp w reaches lanes 32*(w%4) .. +31
     const int row = quad * 32 + lane;
     const int tid = threadIdx.x - 64;  // 0..127 over the four epilogue warps
-    if constexpr (C::SWAP_ONLY) {
+    if constexpr (FUSED) {
       // (a wait that gave up set the abort flag; the epilogue below then does no work)
-      if (fused_q) quantize_operand_b<C, GROUPED>(p, tb, work0, crank, smem, full, empty, wc, tid);
+      quantize_operand_b<C, GROUPED>(p, tb, work0, crank, smem, full, empty, wc, tid);
     }
     // alpha is read by one thread and shared: a load left to each thread's first use was
     // scheduled there, putting a full memory latency (~1400 cycles) in front of the stores.
