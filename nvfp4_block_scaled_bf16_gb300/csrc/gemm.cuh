@@ -9,7 +9,7 @@
 // the 128 rows of a 512-byte tile from 4 tensor-memory columns of each 32-lane quadrant: lane
 // 32q+i, column j holds the 4 bytes at tile offset 16*i + 4*j, the same in every quadrant.
 //
-// CTA = 10 warps:
+// CTA = 10 warps (11 in CTA pairs):
 //   warp 0      TMA producer (one thread issues every copy): A/B tiles (128-byte swizzle) and
 //               scale chunks (bulk copies) into a STAGES-deep shared-memory ring, one mbarrier
 //               pair per stage.  A single-tile CTA whose K slice fits the ring ("resident")
@@ -21,13 +21,15 @@
 //               the scale writers, and after the last K stage of a tile the accumulator to the
 //               epilogue;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, alpha * acc in fp32, one RNE
-//               conversion to bf16, 256-bit stores;
+//               conversion to bf16, 256-bit stores (in the fused-quantisation kernels they
+//               first quantise the bf16 activation into the operand-B stages);
 //   warps 6..9  scale writers: each reads the stage's scale tiles from shared memory and
 //               writes them into its own quadrant of a tensor-memory scale slot with
 //               tcgen05.st (SF_SLOTS slots in a ring; a resident CTA fills one slot per stage
 //               with a single hand-off to the MMA lane), keeping those writes off the tensor pipe
 //               (a tcgen05.cp of one 512-byte tile occupies the pipe about as long as 40 % of a
-//               128x256x64 MMA).
+//               128x256x64 MMA);
+//   warp 10     (pairs only) copies the scales into a ring of their own, ahead of the operands.
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
 //
 // CTA pairs (PAIR, 256 x 256 tiles for large M): a cluster of two CTAs runs cta_group::2 MMAs
