@@ -20,7 +20,7 @@ Each function cites the passage it follows as "page title, section".  Sources:
   text (the 6-D strided scale view over the 128x4-swizzled buffer).
 * [vLLM-51158] vLLM PR 51158 "Enable CUTLASS MXFP4 W4A4 MoE on SM12x".
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 quantiser operation order, sign of zero for e2m1, nibble order, e4m3
 saturation and the MXFP4 scale rounding (round up to a power of two).
 Parity pins: every function here is pinned by tests/test_oracle_*.py.

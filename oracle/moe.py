@@ -5,7 +5,7 @@ scaled_fp4_experts_quant, silu_and_mul_scaled_fp4_experts_quant with the argumen
 input_offset_by_experts and output_scale_offset_by_experts, and cutlass_fp4_group_mm);
 vLLM PR 51158 "Enable CUTLASS MXFP4 W4A4 MoE on SM12x", "Changes" (experts quantise, grouped
 GEMM, CutlassExpertsMxfp4 around them).  The pages give names and arguments only; the readings
-taken here (each in the design doc):
+taken here:
 
 * routing order: rows are grouped by expert; inside an expert, (token, slot) pairs keep their
   row-major order (a stable counting sort of the flattened top-k ids);
