@@ -1109,8 +1109,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         tmem_ld_32x32b_x32(t_base + 32 * c, r);
         tmem_ld_wait();
         if (C::SWAP_ONLY && p.splits > 1) {
+          // (the reduction reads the valid columns only)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i)
+            if (32 * c + i < t.cols) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
         } else if (sk_part) {
           float *dst = slot + (c * 128 + row) * 32;
 #pragma unroll
@@ -1286,7 +1288,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           }
         }
       }
-      cluster_sync();
+      // no CTA leaves while another may still read its partial; those reads are complete here
+      // (their sums are stored), so the arrive publishes nothing
+      cluster_sync_relaxed();
     }
   }
 
