@@ -74,7 +74,8 @@ enum : int {
   kSiteEpilogue = 6     // epilogue: accumulator complete
 };
 
-template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1, bool PAIR_ = false>
+template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1, bool PAIR_ = false,
+          int MAX_EXPERTS_ = 1024>
 struct GemmCfg {
   static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
   static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
@@ -117,7 +118,7 @@ struct GemmCfg {
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int RED_BYTES = BM * BN * 4;  // partial tile: cluster split-K buffer, stream-K slot
-  static constexpr int MAX_EXPERTS = 1024;
+  static constexpr int MAX_EXPERTS = MAX_EXPERTS_;  // grouped: expert tables in shared memory
   static constexpr int TABLE_BYTES = 3 * (MAX_EXPERTS + 1) * 4;
   static constexpr int CTRL_BYTES = 512;
   // A pair adds warp 10, which copies the scales into a ring of their own (SF_STAGES deep) ahead

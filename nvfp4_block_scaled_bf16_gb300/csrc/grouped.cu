@@ -16,7 +16,8 @@ using namespace nvfp4;
 namespace {
 constexpr int kGroupedBN = 128;
 using GroupedCfg = GemmCfg<kGroupedBN, 6, true>;       // MXFP4: 34 KB stages
-using GroupedCfgNv = GemmCfg<kGroupedBN, 5, false>;    // NVFP4: 36 KB stages (+ expert tables)
+// NVFP4: 36 KB stages; expert tables for up to 512 experts leave room for a 6-deep ring
+using GroupedCfgNv = GemmCfg<kGroupedBN, 6, false, true, 1, false, 512>;
 static_assert(GroupedCfgNv::smem_bytes(true) <= 232448 && GroupedCfg::smem_bytes(true) <= 232448, "smem");
 
 // Shared by both grouped entry points: argument checks, tensor maps, launch.

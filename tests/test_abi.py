@@ -138,6 +138,7 @@ def test_quantizers_reject_bad_arguments_without_a_device(lib):
     assert L.mxfp4_quantize(_c(X), 4, 64, 64, None, 0, _c(Q), _c(S), 16, 0, None) == 1   # sf too small
     assert L.mxfp4_quantize(_c(X), 4, 64, 64, _c(X), 2000, _c(Q), _c(S), 1 << 30, 0, None) == 1
     assert L.mxfp4_grouped_gemm(_c(X), _c(S), _c(X), 0, _c(X), _c(S), None, _c(Q), 4, 64, 64, 0, None) == 1
+    assert L.nvfp4_grouped_gemm(_c(X), _c(S), _c(X), 513, _c(X), _c(S), None, _c(Q), 4, 64, 64, 0, None) == 1
     assert L.sf_swizzle(_c(X), _c(Q), -1, 4, 1, None) == 1
     assert L.sf_swizzle(_c(X), _c(Q), 4, 4, 7, None) == 1
 
