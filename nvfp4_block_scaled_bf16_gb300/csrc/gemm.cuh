@@ -134,8 +134,16 @@ struct GemmCfg {
   static constexpr int SFA_REGION = B_REGION + STAGES * B_BYTES;
   static constexpr int SFB_REGION = SFA_REGION + SF_STAGES * SFA_BYTES;
   // dynamic shared memory: alignment slack, stage ring, barriers, expert tables (grouped only)
+  // PUSH_RED (32-wide swap-AB tiles, two CTAs per SM; used from 16 tokens on): the cluster
+  // split-K reduction pushes each rank's slice of the partial into that rank's receive buffer
+  // with bulk copies completing on the receiver's own barrier, instead of publishing every
+  // partial with a cluster-scope release and reading it remotely.  The buffer holds one slice per
+  // other rank: with U = BN*32 units of 16 bytes and S <= 8 ranks, (S-1) * ceil(U/S) <= U - U/8
+  // + 7 units; it follows the control block.
+  static constexpr bool PUSH_RED = !MULTI_TILE_ && BN_ == 32;
+  static constexpr int RCV_BYTES = PUSH_RED ? (BN_ * 32 - BN_ * 32 / 8 + 8) * 16 : 0;
   static constexpr int smem_bytes(bool grouped) {
-    return 1024 + RING_BYTES + CTRL_BYTES + (grouped ? TABLE_BYTES : 0);
+    return 1024 + RING_BYTES + CTRL_BYTES + RCV_BYTES + (grouped ? TABLE_BYTES : 0);
   }
   static constexpr uint32_t IDESC = idesc_block_scaled(PAIR ? 2 * BM : BM, BN, MX, 0);
   // arrivals on the scale-slot-written and accumulator-drained barriers (both CTAs of a pair
@@ -143,7 +151,7 @@ struct GemmCfg {
   static constexpr int SLOT_ARRIVALS = PAIR ? 8 : 4;
   static constexpr int ACC_ARRIVALS = PAIR ? 8 : 4;
   static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8, "tensor memory budget, scale-slot barriers");
-  static_assert(STAGES <= 8 && SF_STAGES <= 8 && (2 * STAGES + 45) * 8 + 8 * 4 <= CTRL_BYTES,
+  static_assert(STAGES <= 7 && SF_STAGES <= 8 && (2 * STAGES + 46) * 8 + 8 * 4 <= CTRL_BYTES,
                 "barriers and flags fit the control block");
   static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
   static_assert(MIN_BLOCKS == 1 || (MIN_BLOCKS * (smem_bytes(false) + 1024) <= 233472 && MIN_BLOCKS * TMEM_COLS <= 512),
@@ -598,7 +606,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   uint64_t *sf_full = drain + 1;       // pair: scale ring slot landed
   uint64_t *sf_empty = sf_full + 8;    // pair: scale ring slot read by the 4 scale writers
   uint64_t *peer_full = sf_empty + 8;  // pair (first CTA): the second CTA's operand stage landed
-  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(peer_full + 8);
+  uint64_t *rbar = peer_full + 8;      // push reduction: this rank's slices received
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(rbar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
   volatile int *issued_count = consumed + 1;  // K stages the producer issued (abort drain)
@@ -611,6 +620,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int crank = C::PAIR ? static_cast<int>(cluster_ctarank()) : 0;  // place in the CTA pair
   constexpr bool fused_q = FUSED;  // operand B quantised in-kernel
+  // split-K reduction by pushes (32-wide tiles, at least 16 tokens: with fewer, a slice is a few
+  // units and reading the partials remotely was measured faster); the same on every CTA
+  const bool push_red = C::PUSH_RED && p.splits > 1 && p.n >= 16;
   static_assert(!FUSED || (C::SWAP_ONLY && !GROUPED), "fused quantisation serves the swap-AB plans");
   const WaitCtl wc{p.wait_limit, abort_flag, p.status};
   // The next kernel may launch now: it waits (griddepcontrol.wait) for this grid to complete
@@ -631,6 +643,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       mbar_init(smem_u32(&sfe[q]), 1);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(rbar), 1);
     if constexpr (C::PAIR) {
       for (int j = 0; j < C::SF_STAGES; ++j) {
         mbar_init(smem_u32(&sf_full[j]), 1);
@@ -707,6 +720,11 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   // other's barriers, so both must have initialised theirs
   if constexpr (C::PAIR) cluster_sync();
   else __syncthreads();
+  // push reduction: every rank's receive barrier is initialised before any slice is pushed (the
+  // matching wait comes after the mainloop, when this arrive has long completed)
+  if constexpr (C::PUSH_RED) {
+    if (push_red) cluster_arrive_relaxed();
+  }
   const Work work0 = make_work<GROUPED, C::PAIR>(p, GROUPED ? tb.tp[p.experts] : 0);
   // The loader (warp 0) starts right away; warp 1 allocates tensor memory meanwhile and a named
   // barrier among warps 1..9 (the tensor-memory users) publishes its address.
@@ -1197,6 +1215,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   }
 
   tc_fence_before();  // order this warp's tcgen05 work before the barrier (dealloc follows it)
+  if (push_red) fence_proxy_async_smem();  // partials -> visible to the bulk copies
   __syncthreads();
   if (*abort_flag) {
     // Drain: wait (bounded) for copies still landing in shared memory and for outstanding
@@ -1231,6 +1250,58 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
 
   if constexpr (!GROUPED && C::SWAP_ONLY) {
     if (p.splits > 1) {
+      if (push_red) {
+        // Split-K reduction by pushes: CTA `rank` reduces the contiguous 1/splits of the valid
+        // units (float4 groups of the column-major partial) [u0, u1); every other rank copies
+        // that slice of its partial into this CTA's receive buffer (slot s for source rank s
+        // below this one, s - 1 above), the copies completing on this CTA's rbar; the sum runs
+        // in rank order, as below.
+        cluster_wait();
+        const int rank = static_cast<int>(cluster_ctarank()), S = p.splits;
+        Work w = work0;
+        Seg sg{};
+        w.next(p, sg);
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg.tile, crank);
+        const float alpha = *alpha_s;
+        const int units = min(t.cols, C::BN) * 32;
+        const int slot = (units + S - 1) / S;  // units of the largest slice
+        const int u0 = rank * units / S, u1 = (rank + 1) * units / S;
+        const uint32_t red0 = smem_u32(smem), rcv0 = smem_u32(ctrl + C::CTRL_BYTES);
+        if (threadIdx.x == 0) {
+          mbar_arrive_expect_tx(smem_u32(rbar), static_cast<uint32_t>((S - 1) * (u1 - u0) * 16));
+          for (int r = 0; r < S; ++r) {
+            const int a0 = r * units / S, a1 = (r + 1) * units / S;
+            if (r != rank && a1 > a0)
+              bulk_copy_to_peer(map_to_rank(rcv0 + static_cast<uint32_t>((rank < r ? rank : rank - 1) * slot * 16), r),
+                                red0 + a0 * 16,
+                                static_cast<uint32_t>((a1 - a0) * 16), map_to_rank(smem_u32(rbar), r));
+          }
+        }
+        if (mbar_wait(smem_u32(rbar), 0, wc, kSiteEpilogue)) {
+          const float4 *own = reinterpret_cast<const float4 *>(smem);
+          const float4 *rcv = reinterpret_cast<const float4 *>(ctrl + C::CTRL_BYTES);
+          for (int u = u0 + static_cast<int>(threadIdx.x); u < u1; u += C::THREADS) {
+            float4 v = rank == 0 ? own[u] : rcv[u - u0];  // (source 0 sits in slot 0)
+            for (int s2 = 1; s2 < S; ++s2) {
+              const float4 q = s2 == rank ? own[u] : rcv[(s2 < rank ? s2 : s2 - 1) * slot + (u - u0)];
+              v.x += q.x;
+              v.y += q.y;
+              v.z += q.z;
+              v.w += q.w;
+            }
+            const int c = (u * 4) / 128, r0 = (u * 4) % 128;
+            if (r0 < t.rows) {
+              uint2 pk;  // (swap-AB: the output row is the token, the 4 values are weight rows)
+              pk.x = pack_bf16x2(__fmul_rn(alpha, v.x), __fmul_rn(alpha, v.y));
+              pk.y = pack_bf16x2(__fmul_rn(alpha, v.z), __fmul_rn(alpha, v.w));
+              *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
+            }
+          }
+        }
+        // the copies out of this CTA's partial have completed (every receiver saw its slices)
+        // before any CTA leaves; the arrive publishes nothing
+        cluster_sync_relaxed();
+      } else {
       // Split-K reduction across the cluster.  The partial tile is stored column-major
       // (128 rows per column, a 4-row group per float4 unit); only the units of the tile's
       // valid columns are reduced, CTA `rank` taking a contiguous 1/splits of them.  Every
@@ -1292,6 +1363,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       // no CTA leaves while another may still read its partial; those reads are complete here
       // (their sums are stored), so the arrive publishes nothing
       cluster_sync_relaxed();
+      }
     }
   }
 
