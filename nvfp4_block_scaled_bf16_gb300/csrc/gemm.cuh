@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   uint64_t *empty = full + C::STAGES;
   uint64_t *accf = empty + C::STAGES;
   uint64_t *acce = accf + 2;
-  uint64_t *sff = acce + 2;           // scale slot written (4 scale-writer warps arrive)
+  uint64_t *sff = acce + 2;           // scale slot written (the scale writers arrive: 4, 8 in a pair)
   uint64_t *sfe = sff + 8;            // scale slot free (MMA commit)
   uint64_t *drain = sfe + 8;
   uint64_t *sf_full = drain + 1;       // pair: scale ring slot landed
