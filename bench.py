@@ -167,6 +167,36 @@ class Workload:
         for f in self.launches:
             f()
 
+    def pack_transfers(self, align: int = 256, device: str = "cuda"):
+        """Moves the step's inputs into one device buffer (each tensor becomes a view at an
+        `align`-byte offset) with one pinned host image, and its outputs likewise, so that a step
+        crosses the host link with one copy each way instead of one per tensor.  Must run before
+        the launches are captured: the launch closures hold these tensor objects, which `set_`
+        re-points in place.  Returns (h2d_bytes, d2h_bytes) per step."""
+        moved = []
+        for pairs, dev_at in ((self.h2d, 0), (self.d2h, 1)):
+            if not pairs:
+                moved.append(None)
+                continue
+            offs, total = [], 0
+            for p in pairs:
+                t = p[dev_at]
+                assert t.is_contiguous()
+                offs.append(total)
+                total += -(-t.numel() * t.element_size() // align) * align
+            dbuf = torch.empty(total, dtype=torch.uint8, device=device)
+            hbuf = torch.empty(total, dtype=torch.uint8)
+            hbuf = hbuf.pin_memory() if device == "cuda" else hbuf
+            for p, o in zip(pairs, offs):
+                for t, buf in ((p[dev_at], dbuf), (p[1 - dev_at], hbuf)):
+                    nb = t.numel() * t.element_size()
+                    slot = buf[o:o + nb].view(t.dtype).view(t.shape)
+                    slot.copy_(t)
+                    t.set_(slot)
+            moved.append((dbuf, hbuf))
+        self.h2d_buf, self.d2h_buf = moved
+        return tuple(0 if b is None else b[0].numel() for b in moved)
+
 
 def _gs(x: torch.Tensor) -> float:
     return float(np.float32(2688.0) / np.float32(x.float().abs().max().item()))
@@ -459,6 +489,7 @@ def run_ours(args, dist_on, rank, world):
     else:
         wl = MAKERS[args.workload](nv)
     flush = L2Flush()
+    h2d_bytes, d2h_bytes = wl.pack_transfers()
     step_graph = capture(wl.launches)
     gemm_graph = capture(wl.gemm_launches)
     for _ in range(args.warmup):
@@ -484,18 +515,18 @@ def run_ours(args, dist_on, rank, world):
     quant_ms = max(0.0, ms - gemm_mean)
 
     # ---- end to end through the public API with host buffers
+    # (inputs packed into one pinned image and one device buffer, outputs likewise: one copy each
+    # way per step, the bytes counted from those buffers)
     def h2d():
-        for dev_t, host_t in wl.h2d:
-            dev_t.copy_(host_t, non_blocking=True)
+        dbuf, hbuf = wl.h2d_buf
+        dbuf.copy_(hbuf, non_blocking=True)
 
     def d2h():
-        for host_t, dev_t in wl.d2h:
-            host_t.copy_(dev_t, non_blocking=True)
+        dbuf, hbuf = wl.d2h_buf
+        hbuf.copy_(dbuf, non_blocking=True)
 
     e2e_ms_list = timed_replays(step_graph, max(3, min(args.steps, 50)), flush, before=h2d, after=d2h)
     e2e_ms = max_over_ranks(statistics.mean(e2e_ms_list), dist_on)
-    h2d_bytes = sum(t.numel() * t.element_size() for _, t in wl.h2d)
-    d2h_bytes = sum(t.numel() * t.element_size() for t, _ in wl.d2h)
 
     hbm, bf16, peak_kind = peaks()
     tflops = wl.flops * world / (ms * 1e-3) / 1e12

@@ -1,0 +1,53 @@
+"""Host logic of bench.py that needs no GPU: packing a step's transfers into one buffer each way."""
+import os
+import sys
+
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def _workload():
+    wl = bench.Workload(None, "t")
+    g = torch.Generator().manual_seed(0)
+    ins = [torch.randn(3, 5, generator=g).to(torch.bfloat16), torch.arange(7, dtype=torch.int32),
+           torch.rand(2, 9, generator=g)]
+    for t in ins:
+        wl.h2d.append((torch.empty_like(t), t.clone()))        # (device side, host side)
+    outs = [torch.full((4, 3), 2.5).to(torch.bfloat16), torch.ones(1, dtype=torch.int64)]
+    for t in outs:
+        wl.d2h.append((torch.empty_like(t), t.clone()))        # (host side, device side)
+    return wl, ins, outs
+
+
+def test_pack_keeps_contents_and_aligns_views():
+    wl, ins, outs = _workload()
+    dev_in = [p[0] for p in wl.h2d]
+    hi, ho = wl.pack_transfers(align=256, device="cpu")
+    assert hi == 3 * 256 and ho == 2 * 256
+    dbuf, hbuf = wl.h2d_buf
+    base_d, base_h = dbuf.data_ptr(), hbuf.data_ptr()
+    for i, ((d, h), want) in enumerate(zip(wl.h2d, ins)):
+        assert d is dev_in[i]                                  # same objects: closures still see them
+        assert d.data_ptr() - base_d == 256 * i and h.data_ptr() - base_h == 256 * i
+        assert torch.equal(h, want) and d.shape == want.shape and d.dtype == want.dtype
+    odbuf, ohbuf = wl.d2h_buf
+    for i, ((h, d), want) in enumerate(zip(wl.d2h, outs)):
+        assert d.data_ptr() - odbuf.data_ptr() == 256 * i and h.data_ptr() - ohbuf.data_ptr() == 256 * i
+        assert torch.equal(d, want)
+
+
+def test_one_copy_each_way_moves_every_tensor():
+    wl, ins, outs = _workload()
+    wl.pack_transfers(align=256, device="cpu")
+    dbuf, hbuf = wl.h2d_buf
+    dbuf.zero_()
+    dbuf.copy_(hbuf)                                           # the step's single input copy
+    for (d, _), want in zip(wl.h2d, ins):
+        assert torch.equal(d, want)
+    for (_, d), v in zip(wl.d2h, (7.0, 3)):
+        d.fill_(v)                                             # a kernel writing its output
+    odbuf, ohbuf = wl.d2h_buf
+    ohbuf.copy_(odbuf)                                         # the step's single output copy
+    assert torch.all(wl.d2h[0][0] == 7.0) and torch.all(wl.d2h[1][0] == 3)
