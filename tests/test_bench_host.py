@@ -51,3 +51,14 @@ def test_one_copy_each_way_moves_every_tensor():
     odbuf, ohbuf = wl.d2h_buf
     ohbuf.copy_(odbuf)                                         # the step's single output copy
     assert torch.all(wl.d2h[0][0] == 7.0) and torch.all(wl.d2h[1][0] == 3)
+
+
+def test_transfer_groups_follow_readers_and_writers():
+    wl, ins, outs = _workload()
+    wl.launches = [None] * 5
+    wl.h2d_at = [0, 0, 3]              # the first two inputs are read by launch 0: one copy
+    wl.d2h_after = [2]                 # the second output defaults to the last launch
+    wl.pack_transfers(align=256, device="cpu")
+    gin, gout = wl.transfer_groups()
+    assert gin == [(0, 0, 512), (3, 512, 768)]
+    assert gout == [(2, 0, 256), (4, 256, 512)]
