@@ -351,7 +351,12 @@ nvfp4_status_t nvfp4_sf_convert_layout(const uint8_t *src, uint8_t *dst, int64_t
  * bounded pipeline wait gave up, a grouped GEMM found malformed row offsets or a MoE step found
  * an index out of range.  Returns NVFP4_ERR_INVALID_ARG for malformed offsets or indices, NVFP4_ERR_TIMEOUT if a
  * kernel timed out since the last check, NVFP4_ERR_CUDA if the synchronisation failed,
- * NVFP4_OK otherwise. */
+ * NVFP4_OK otherwise.
+ * The word is one per device, shared by every stream and thread: the call reports what any of
+ * this library's kernels on the current device recorded since the previous check, and a bit
+ * that a kernel on another, still-running stream sets between the read and the clear is lost.
+ * For an exact account, call it when no other stream of the device has this library's work in
+ * flight. */
 nvfp4_status_t nvfp4_check_status(nvfp4_stream_t stream);
 
 #ifdef __cplusplus

@@ -2,6 +2,7 @@
 // maps, and the size queries of the C ABI.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -18,7 +19,7 @@ thread_local char t_msg[512] = "";
 
 constexpr int kMaxDevices = 64;
 struct DevState {
-  bool ready = false;
+  std::atomic<bool> ready{false};  // set (release) after the fields below are filled in
   bool ok = false;
   DeviceInfo info{};
   char why[200] = "";
@@ -55,9 +56,9 @@ nvfp4_status_t current_device(DeviceInfo *out) {
   if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
   DevState &st = g_dev[dev];
-  if (!st.ready) {
+  if (!st.ready.load(std::memory_order_acquire)) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!st.ready) {
+    if (!st.ready.load(std::memory_order_relaxed)) {
       int major = 0, minor = 0, sms = 0;
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -77,7 +78,7 @@ nvfp4_status_t current_device(DeviceInfo *out) {
         st.info.sm_count = sms;
         st.info.status = static_cast<unsigned int *>(status);
       }
-      st.ready = true;
+      st.ready.store(true, std::memory_order_release);
     }
   }
   if (!st.ok) return fail(NVFP4_ERR_UNSUPPORTED_DEVICE, "%s", st.why);
@@ -90,9 +91,8 @@ long long wait_limit(uint32_t flags) {
   return (flags & NVFP4_FLAG_DEBUG_TIMEOUT) ? 40000000LL : 20000000000LL;
 }
 
-nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes,
-                                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
-                                 uint32_t box_rows, bool swizzle128) {
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime (no -lcuda needed).
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   std::call_once(g_encode_once, [] {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -101,12 +101,19 @@ nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t in
     if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  return g_encode;
+}
+
+nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner_bytes,
+                                 uint64_t rows, uint64_t row_stride_bytes, uint32_t box_inner,
+                                 uint32_t box_rows, bool swizzle128) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (!encode) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint64_t dims[2] = {inner_bytes, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -119,21 +126,14 @@ nvfp4_status_t encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t in
 
 nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_t k_bytes, uint64_t rows,
                                      uint32_t box_rows, uint32_t box_stages) {
-  std::call_once(g_encode_once, [] {
-    void *fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                    cudaEnableDefault, &q);
-    if (g_encode_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (!encode) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   if (k_bytes % 128 != 0) return fail(NVFP4_ERR_INVALID_ARG, "stage view needs K %% 256 == 0");
   cuuint64_t dims[3] = {128, rows, k_bytes / 128};
   cuuint64_t strides[2] = {k_bytes, 128};
   cuuint32_t box[3] = {128, box_rows, box_stages};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
