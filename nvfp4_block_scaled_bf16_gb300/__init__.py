@@ -2,7 +2,9 @@
 
 Thin ctypes marshalling over the C ABI in include/nvfp4.h: each function here has the name of
 the C entry point it calls, takes torch CUDA tensors, allocates missing outputs with
-torch.empty, and passes raw pointers and the current CUDA stream.  All arithmetic runs in the
+torch.empty, checks what the library cannot see behind a bare pointer (device, dtype,
+contiguity, size of every buffer), and passes raw pointers and the current CUDA stream.  All
+arithmetic runs in the
 library's CUDA kernels; there is no CPU fallback.  Importing fails if libnvfp4.so is missing
 (build it with ``python nvfp4_block_scaled_bf16_gb300/build.py``).
 """
@@ -94,13 +96,43 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t, dtype, name, dim=None):
+def _check_device(t, name):
+    """The library launches on the current CUDA device; every tensor must live there."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    if t.get_device() != cur:
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, the current device is cuda:{cur}")
+
+
+def _need(t, dtype, name, dim=None):
+    _check_device(t, name)
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if dim is not None and t.dim() != dim:
         raise ValueError(f"{name} must have {dim} dimensions")
+
+
+def _room(t, dtype, name, numel):
+    """A buffer the kernels read or write `numel` elements of, densely from its first element (the
+    library sees only the pointer, so its size is checked here)."""
+    _need(t, dtype, name)
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+
+
+def _contig(t, stream):
+    """`t` with dense rows.  A copy is made on the launch stream, so that the caching allocator
+    cannot hand its memory out again before that stream's kernel has read it."""
+    if t.is_contiguous():
+        return t
+    if stream is None:
+        return t.contiguous()
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(stream)
+    with torch.cuda.stream(s):
+        return t.contiguous()
 
 
 def sf_bytes(rows: int, k: int, sf_vec: int = 16) -> int:
@@ -154,6 +186,8 @@ def nvfp4_quantize(x, gs, q=None, sf=None, flags: int = 0, stream=None):
         q = torch.empty((m, k // 2), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.empty(sf_bytes(m, k, 16), dtype=torch.uint8, device=x.device)
+    _room(q, torch.uint8, "q", m * (k // 2))
+    _room(sf, torch.uint8, "sf", sf_bytes(m, k, 16))
     _check(_lib.nvfp4_quantize(_ptr(x), m, k, x.stride(0), _ptr(gs), _ptr(q), _ptr(sf), flags, _stream(stream)))
     return q, sf
 
@@ -173,6 +207,8 @@ def mxfp4_quantize(x, row_offsets=None, q=None, sf=None, flags: int = 0, stream=
         q = torch.empty((t, k // 2), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.zeros(need, dtype=torch.uint8, device=x.device)
+    _room(q, torch.uint8, "q", t * (k // 2))
+    _room(sf, torch.uint8, "sf", 0)            # its capacity goes to the library, which checks it
     _check(_lib.mxfp4_quantize(_ptr(x), t, k, x.stride(0), _ptr(row_offsets), experts, _ptr(q), _ptr(sf),
                                sf.numel(), flags, _stream(stream)))
     return q, sf
@@ -199,12 +235,13 @@ def nvfp4_gemm(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=None, works
         raise ValueError("scale buffers are too small")
     if d is None:
         d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _room(d, torch.bfloat16, "d", m * n)
     if workspace is None and m > 0:
         need = gemm_workspace_size(m, n, 2 * kh)
         if need:
             workspace = _default_workspace(need, a.device)
     if workspace is not None:
-        _need(workspace, torch.uint8, "workspace")
+        _room(workspace, torch.uint8, "workspace", 0)   # the library checks its size
     _check(_lib.nvfp4_gemm(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
                            _ptr(workspace), 0 if workspace is None else workspace.numel(), flags,
                            _stream(stream)))
@@ -231,6 +268,7 @@ def nvfp4_quantize_gemm(x, gs, b, sfb, alpha, d=None, flags: int = 0, stream=Non
         raise ValueError("sfb is too small")
     if d is None:
         d = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    _room(d, torch.bfloat16, "d", m * n)
     _check(_lib.nvfp4_quantize_gemm(_ptr(x), x.stride(0), _ptr(gs), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, k,
                                     None, 0, flags, _stream(stream)))
     return d
@@ -255,6 +293,7 @@ def nvfp4_gemm_noalloc(a, sfa, b, sfb, alpha, d=None, flags: int = 0, stream=Non
         raise ValueError("scale buffers are too small")
     if d is None:
         d = torch.empty((m, n), dtype=torch.bfloat16, device=a.device)
+    _room(d, torch.bfloat16, "d", m * n)
     _check(_lib.nvfp4_gemm_noalloc(_ptr(a), _ptr(sfa), _ptr(b), _ptr(sfb), _ptr(alpha), _ptr(d), m, n, 2 * kh,
                                    flags, _stream(stream)))
     return d
@@ -269,8 +308,15 @@ def mxfp4_grouped_gemm(a, sfa, row_offsets, b, sfb, alpha=None, d=None, flags: i
     experts, n, kb = b.shape
     if kb != kh or row_offsets.numel() != experts + 1:
         raise ValueError("shape mismatch")
+    if not b.is_contiguous():
+        raise ValueError("b must be contiguous")
+    _need(sfa, torch.uint8, "sfa")
+    _room(sfb, torch.uint8, "sfb", experts * sf_bytes(n, 2 * kh, 32))
+    if alpha is not None:
+        _room(alpha, torch.float32, "alpha", 1)
     if d is None:
         d = torch.empty((t, n), dtype=torch.bfloat16, device=a.device)
+    _room(d, torch.bfloat16, "d", t * n)
     _check(_lib.mxfp4_grouped_gemm(_ptr(a), _ptr(sfa), _ptr(row_offsets), experts, _ptr(b), _ptr(sfb),
                                    _ptr(alpha), _ptr(d), t, n, 2 * kh, flags, _stream(stream)))
     return d
@@ -278,19 +324,22 @@ def mxfp4_grouped_gemm(a, sfa, row_offsets, b, sfb, alpha=None, d=None, flags: i
 
 def sf_swizzle(src, rows: int, cols: int, to_swizzled: bool = True, dst=None, stream=None):
     """Row-major scale bytes [rows, cols] <-> 128x4 swizzled buffer."""
-    _need(src, torch.uint8, "src")
+    padded = (-(-rows // 128) * 128) * (-(-cols // 4) * 4)
+    _room(src, torch.uint8, "src", rows * cols if to_swizzled else padded)
     if dst is None:
-        n = (-(-rows // 128) * 128) * (-(-cols // 4) * 4) if to_swizzled else rows * cols
-        dst = torch.empty(n, dtype=torch.uint8, device=src.device)
+        dst = torch.empty(padded if to_swizzled else rows * cols, dtype=torch.uint8, device=src.device)
+    _room(dst, torch.uint8, "dst", padded if to_swizzled else rows * cols)
     _check(_lib.sf_swizzle(_ptr(src), _ptr(dst), rows, cols, 1 if to_swizzled else 0, _stream(stream)))
     return dst
 
 
 def sf_convert_layout(src, rows: int, cols: int, to_sm103: bool = True, dst=None, stream=None):
     """Swizzled NVFP4 scale buffer: 128x4 ("SM100") layout <-> SM103 layout."""
-    _need(src, torch.uint8, "src")
+    padded = (-(-rows // 128) * 128) * (-(-cols // 4) * 4)
+    _room(src, torch.uint8, "src", padded)
     if dst is None:
         dst = torch.empty_like(src)
+    _room(dst, torch.uint8, "dst", padded)
     _check(_lib.nvfp4_sf_convert_layout(_ptr(src), _ptr(dst), rows, cols, 1 if to_sm103 else 0, _stream(stream)))
     return dst
 
@@ -310,7 +359,7 @@ def moe_sort_by_expert(topk_ids, num_experts: int, out=None, workspace=None, fla
     pos int32 [T, topk]); stable: (token, slot) order inside an expert.  `out` may pass the
     three output tensors to fill."""
     _need(topk_ids, torch.int32, "topk_ids", 2)
-    topk_ids = topk_ids.contiguous()
+    topk_ids = _contig(topk_ids, stream)
     T, topk = topk_ids.shape
     dv = topk_ids.device
     if out is None:
@@ -318,8 +367,12 @@ def moe_sort_by_expert(topk_ids, num_experts: int, out=None, workspace=None, fla
                torch.empty(T * topk, dtype=torch.int32, device=dv),
                torch.empty((T, topk), dtype=torch.int32, device=dv))
     ro, src, pos = out
+    _room(ro, torch.int64, "row_offsets", num_experts + 1)
+    _room(src, torch.int32, "src_rows", T * topk)
+    _room(pos, torch.int32, "pos", T * topk)
     if workspace is None:
         workspace = torch.empty(max(1, moe_sort_workspace_size(T, num_experts) // 4), dtype=torch.int32, device=dv)
+    _room(workspace, torch.int32, "workspace", 0)        # its size in bytes goes to the library
     _check(_lib.moe_sort_by_expert(_ptr(topk_ids), T, topk, num_experts, _ptr(ro), _ptr(src), _ptr(pos),
                                    _ptr(workspace), workspace.numel() * 4, flags, _stream(stream)))
     return ro, src, pos
@@ -335,6 +388,9 @@ def moe_gather_rows(x, src_rows, out=None, flags: int = 0, stream=None):
     rows = src_rows.numel()
     if out is None:
         out = torch.empty((rows, h), dtype=torch.bfloat16, device=x.device)
+    if not src_rows.is_contiguous():
+        raise ValueError("src_rows must be contiguous")
+    _room(out, torch.bfloat16, "out", rows * h)
     _check(_lib.moe_gather_rows(_ptr(x), T, h, x.stride(0), _ptr(src_rows), rows, _ptr(out), flags, _stream(stream)))
     return out
 
@@ -350,6 +406,10 @@ def nvfp4_quantize_experts(x, row_offsets, gs, q=None, sf=None, flags: int = 0, 
         q = torch.empty((t, k // 2), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.empty(expert_sf_bytes(t, experts, k), dtype=torch.uint8, device=x.device)
+    _room(row_offsets, torch.int64, "row_offsets", experts + 1)
+    _room(gs, torch.float32, "gs", experts)
+    _room(q, torch.uint8, "q", t * (k // 2))
+    _room(sf, torch.uint8, "sf", 0)            # its capacity goes to the library, which checks it
     _check(_lib.nvfp4_quantize_experts(_ptr(x), t, k, x.stride(0), _ptr(row_offsets), experts, _ptr(gs), _ptr(q),
                                        _ptr(sf), sf.numel(), flags, _stream(stream)))
     return q, sf
@@ -367,6 +427,10 @@ def nvfp4_silu_mul_quantize_experts(x, row_offsets, gs, q=None, sf=None, flags: 
         q = torch.empty((t, inter // 2), dtype=torch.uint8, device=x.device)
     if sf is None:
         sf = torch.empty(expert_sf_bytes(t, experts, inter), dtype=torch.uint8, device=x.device)
+    _room(row_offsets, torch.int64, "row_offsets", experts + 1)
+    _room(gs, torch.float32, "gs", experts)
+    _room(q, torch.uint8, "q", t * (inter // 2))
+    _room(sf, torch.uint8, "sf", 0)
     _check(_lib.nvfp4_silu_mul_quantize_experts(_ptr(x), t, inter, x.stride(0), _ptr(row_offsets), experts, _ptr(gs),
                                                 _ptr(q), _ptr(sf), sf.numel(), flags, _stream(stream)))
     return q, sf
@@ -381,8 +445,15 @@ def nvfp4_grouped_gemm(a, sfa, row_offsets, b, sfb, alpha=None, d=None, flags: i
     experts, n, kb = b.shape
     if kb != kh or row_offsets.numel() != experts + 1 or (alpha is not None and alpha.numel() != experts):
         raise ValueError("shape mismatch")
+    if not b.is_contiguous():
+        raise ValueError("b must be contiguous")
+    _need(sfa, torch.uint8, "sfa")
+    _room(sfb, torch.uint8, "sfb", experts * sf_bytes(n, 2 * kh, 16))
+    if alpha is not None:
+        _room(alpha, torch.float32, "alpha", experts)
     if d is None:
         d = torch.empty((t, n), dtype=torch.bfloat16, device=a.device)
+    _room(d, torch.bfloat16, "d", t * n)
     _check(_lib.nvfp4_grouped_gemm(_ptr(a), _ptr(sfa), _ptr(row_offsets), experts, _ptr(b), _ptr(sfb), _ptr(alpha),
                                    _ptr(d), t, n, 2 * kh, flags, _stream(stream)))
     return d
@@ -393,11 +464,17 @@ def moe_combine(y, pos, weights, out=None, flags: int = 0, stream=None):
     _need(y, torch.bfloat16, "y", 2)
     _need(pos, torch.int32, "pos", 2)
     _need(weights, torch.float32, "weights", 2)
+    if not y.is_contiguous():
+        raise ValueError("y must be contiguous")
     rows, h = y.shape
     T, topk = pos.shape
+    if tuple(weights.shape) != (T, topk):
+        raise ValueError(f"weights must have shape {(T, topk)}, got {tuple(weights.shape)}")
+    pos, weights = _contig(pos, stream), _contig(weights, stream)
     if out is None:
         out = torch.empty((T, h), dtype=torch.bfloat16, device=y.device)
-    _check(_lib.moe_combine(_ptr(y), rows, _ptr(pos.contiguous()), _ptr(weights.contiguous()), T, topk, h, _ptr(out),
+    _room(out, torch.bfloat16, "out", T * h)
+    _check(_lib.moe_combine(_ptr(y), rows, _ptr(pos), _ptr(weights), T, topk, h, _ptr(out),
                             flags, _stream(stream)))
     return out
 
