@@ -4,9 +4,8 @@ Thin ctypes marshalling over the C ABI in include/nvfp4.h: each function here ha
 the C entry point it calls, takes torch CUDA tensors, allocates missing outputs with
 torch.empty, checks what the library cannot see behind a bare pointer (device, dtype,
 contiguity, size of every buffer), and passes raw pointers and the current CUDA stream.  All
-arithmetic runs in the
-library's CUDA kernels; there is no CPU fallback.  Importing fails if libnvfp4.so is missing
-(build it with ``python nvfp4_block_scaled_bf16_gb300/build.py``).
+arithmetic runs in the library's CUDA kernels; there is no CPU fallback.  Importing fails if
+libnvfp4.so is missing (build it with ``python nvfp4_block_scaled_bf16_gb300/build.py``).
 """
 from __future__ import annotations
 
