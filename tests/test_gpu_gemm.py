@@ -119,9 +119,11 @@ def test_decode_sweep_full_size(nv, m):
     assert_within(d, R, tol, f"decode M={m}")
 
 
-@pytest.mark.parametrize("m,n,k", [(1024, 4096, 7168), (4096, 4096, 4096), (128, 7168, 2048)])
+@pytest.mark.parametrize("m,n,k", [(1024, 4096, 7168), (2048, 4096, 7168), (4096, 4096, 7168), (4096, 4096, 4096),
+                                   (128, 7168, 2048)])
 def test_prefill_sampled_rows(nv, m, n, k):
-    """Full-size prefill shapes, checked on whole 128-row blocks at both ends plus seeded rows."""
+    """The five prefill shapes at full size (M = 2048 and 4096 run on CTA pairs), checked on whole
+    128-row blocks at both ends plus seeded rows."""
     ops = nvfp4_operands(m, n, k, 0)
     d = _run(nv, ops)
     rng = np.random.default_rng(m + n + k)
