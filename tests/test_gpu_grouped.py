@@ -72,6 +72,16 @@ def test_moe_gate_up_sampled_experts(nv):
     _check(nv, counts, 1536, 2048, experts_to_check=pick)
 
 
+def test_moe_down_sampled_experts(nv):
+    """The down projection of the same layer: 128 experts, 32768 rows, N=2048, K=768 (three K
+    stages); the smallest and largest experts and six seeded others."""
+    counts = synth.moe_routing(0, 4096, 128, 8)
+    order = torch.argsort(counts)
+    rng = np.random.default_rng(1)
+    pick = sorted(set([int(order[0]), int(order[-1])] + [int(v) for v in rng.integers(0, 128, 6)]))
+    _check(nv, counts, 2048, 768, seed=2, experts_to_check=pick)
+
+
 def test_malformed_row_offsets_are_rejected_on_device(nv):
     """Offsets that do not end at the row count (or decrease) make the kernel do no work and
     nvfp4_check_status report NVFP4_ERR_INVALID_ARG; the output is left untouched."""
