@@ -162,3 +162,50 @@ def test_moe_sort_workspace_size(lib):
     assert lib.moe_sort_workspace_size(1, 8) == 8 * 4
     assert lib.moe_sort_workspace_size(10 ** 6, 16) == 1024 * 16 * 4    # at most 1024 CTAs
     assert lib.moe_sort_workspace_size(-1, 8) == 0
+
+
+def test_moe_steps_reject_bad_arguments_without_a_device(lib):
+    L = lib.lib
+    I, R, P, W, X, O, G, Q, S = (0x10000 * i for i in range(1, 10))   # never dereferenced
+    ws = lib.moe_sort_workspace_size(16, 4)
+    sort = L.moe_sort_by_expert
+    assert sort(_c(I), 16, 33, 4, _c(R), _c(P), _c(P), _c(W), ws, 0, None) == 1      # topk > 32
+    assert sort(_c(I), 16, 2, 1025, _c(R), _c(P), _c(P), _c(W), 1 << 30, 0, None) == 1  # experts > 1024
+    assert sort(_c(I), 16, 2, 4, _c(R), _c(P), _c(P), _c(W), ws - 1, 0, None) == 1   # workspace too small
+    assert "workspace" in lib.last_error()
+    assert sort(_c(I), 16, 2, 4, _c(R), _c(P), _c(P), _c(W), ws, 1 << 2, None) == 1  # flags
+    assert sort(_c(I), 16, 2, 4, None, _c(P), _c(P), _c(W), ws, 0, None) == 1
+    assert sort(_c(I), 16, 2, 4, _c(R + 4), _c(P), _c(P), _c(W), ws, 0, None) == 2   # row_offsets 8-B
+    gather = L.moe_gather_rows
+    assert gather(_c(X), 16, 60, 64, _c(P), 32, _c(O), 0, None) == 1                  # h % 8
+    assert gather(_c(X), 16, 64, 56, _c(P), 32, _c(O), 0, None) == 1                  # ldx < h
+    assert gather(_c(X + 8), 16, 64, 64, _c(P), 32, _c(O), 0, None) == 2
+    assert gather(None, 16, 64, 64, _c(P), 32, _c(O), 0, None) == 1
+    assert gather(None, 0, 64, 64, None, 0, None, 0, None) == 0                        # nothing to gather
+    comb = L.moe_combine
+    assert comb(_c(X), 32, _c(P), _c(G), 16, 0, 64, _c(O), 0, None) == 1              # topk < 1
+    assert comb(_c(X), 32, _c(P), _c(G), 16, 2, 60, _c(O), 0, None) == 1              # h % 8
+    assert comb(_c(X), 32, _c(P), _c(G + 2), 16, 2, 64, _c(O), 0, None) == 2
+    assert comb(_c(X), 32, None, _c(G), 16, 2, 64, _c(O), 0, None) == 1
+    assert comb(None, 0, None, None, 0, 2, 64, None, 0, None) == 0
+    sfb = (128 + 128 * 4) * 16                                                         # t=40, E=4, k=256
+    for f, k, ldx in ((L.nvfp4_quantize_experts, 256, 256), (L.nvfp4_silu_mul_quantize_experts, 256, 512)):
+        assert f(_c(X), 40, 250, ldx, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 3   # k % 16
+        assert f(_c(X), 40, k, ldx - 8, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 2  # ldx too short
+        assert f(_c(X), 40, k, ldx, _c(R), 0, _c(G), _c(Q), _c(S), sfb, 0, None) == 1     # no experts
+        assert f(_c(X), 40, k, ldx, _c(R), 4, _c(G), _c(Q), _c(S), sfb - 1, 0, None) == 1  # sf too small
+        assert f(_c(X), 40, k, ldx, _c(R), 4, _c(G), _c(Q + 4), _c(S), sfb, 0, None) == 2  # q 8-B
+        assert f(_c(X), 40, k, ldx, None, 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 1
+        assert f(None, 0, k, ldx, None, 4, None, None, None, sfb, 0, None) == 0           # no rows
+
+
+def test_noalloc_gemm_refuses_what_nvfp4_gemm_refuses_without_a_device(lib):
+    L = lib.lib
+    A, S, D = 0x10000, 0x20000, 0x30000
+    g = L.nvfp4_gemm_noalloc
+    assert g(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 300, 1024, 16016, 0, None) == 3       # k % 32
+    assert g(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 300, 1000, 16384, 0, None) == 3       # n % 32
+    assert g(_c(A + 16), _c(S), _c(A), _c(S), _c(S), _c(D), 300, 1024, 16384, 0, None) == 2  # split plan, misaligned a
+    assert g(None, _c(S), _c(A), _c(S), _c(S), _c(D), 300, 1024, 16384, 0, None) == 1
+    assert g(_c(A), _c(S), _c(A), _c(S), _c(S), _c(D), 300, 1024, 16384, 1 << 20, None) == 1  # flags
+    assert g(None, None, None, None, None, None, 0, 1024, 1024, 0, None) == 0
