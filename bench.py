@@ -534,18 +534,25 @@ def timed_replays(g, n: int, flush: L2Flush, before=None, after=None) -> list[fl
     return out
 
 
-def barrier(dist_on: bool):
+def barrier(dist_on: bool, device: str = "cuda"):
     if dist_on:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if device == "cuda":
+        torch.cuda.synchronize()
 
 
-def max_over_ranks(v: float, dist_on: bool) -> float:
+def max_over_ranks(v: float, dist_on: bool, device: str = "cuda") -> float:
+    """The slowest rank's time: every rank gets the maximum of `v` over the ranks."""
     if not dist_on:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_max: float) -> float:
+    """Replicas each do `flops_per_rank` in at most `ms_max`: the job's aggregate rate."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
 
 
 def run_ours(args, dist_on, rank, world):
@@ -619,7 +626,7 @@ def run_ours(args, dist_on, rank, world):
     seq_ms = max_over_ranks(seq_ms, dist_on)
 
     hbm, bf16, peak_kind = peaks()
-    tflops = wl.flops * world / (ms * 1e-3) / 1e12
+    tflops = whole_job_tflops(wl.flops, world, ms)
     gemm_gbs = wl.gemm_bytes / (gemm_mean * 1e-3) / 1e9
     fp4_peak_tflops = bf16 * 6.0  # nominal dense FP4 : bf16 ratio 13.5 : 2.25
     gemm_tflops = wl.flops / (gemm_mean * 1e-3) / 1e12
@@ -644,7 +651,7 @@ def run_ours(args, dist_on, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp4 (e2m1) x fp4, fp32 accumulate, bf16 out",
             "data": "synthetic", "config": wl.config,
             "roofline": roof,
-            "e2e": {"value": round(wl.flops * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "e2e": {"value": round(whole_job_tflops(wl.flops, world, e2e_ms), 2), "unit": "TFLOPS",
                     "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                     "copies_overlap_kernels": overlap, "sequential_ms_per_step": round(seq_ms, 5)},
             "gpu_launches": len(wl.launches) * args.steps,

@@ -62,3 +62,41 @@ def test_transfer_groups_follow_readers_and_writers():
     gin, gout = wl.transfer_groups()
     assert gin == [(0, 0, 512), (3, 512, 768)]
     assert gout == [(2, 0, 256), (4, 256, 512)]
+
+
+def _replica_rank(rank, world, port, out):
+    import torch.distributed as dist
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        bench.barrier(True, device="cpu")
+        ms = bench.max_over_ranks(1.0 + rank, True, device="cpu")       # rank 1 is the slow one
+        out.put((rank, ms, bench.whole_job_tflops(2e12, world, ms)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_report_the_slowest_rank_and_the_whole_job():
+    """bench.py --gpus 2 runs two replicas: both see the slower rank's time and the value counts
+    the work of both (gloo on the CPU stands in for NCCL)."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_replica_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.0, 2.0]
+    assert all(abs(r[2] - 2e12 * 2 / 2e-3 / 1e12) < 1e-9 for r in res)      # 2000 TFLOPS
+
+
+def test_reference_arm_prints_only_on_rank_0(capsys):
+    import argparse
+    bench.run_reference(argparse.Namespace(workload="decode", warmup=3, steps=1, gpus=2), rank=1)
+    assert capsys.readouterr().out == ""
