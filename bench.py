@@ -296,7 +296,7 @@ def make_moe(nv):
     wl = Workload(nv, "moe")
     E, T, topk, H, I = 128, 4096, 8, 2048, 768
     counts = synth.moe_routing(0, T, E, topk)
-    ro, _ = synth.moe_offsets(counts)
+    ro = synth.moe_offsets(counts)
     rows = int(ro[-1])
     ro_d = ro.cuda()
     specs = [("gate_up", 2 * I, H, 1), ("down", H, I, 2)]

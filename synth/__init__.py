@@ -146,15 +146,12 @@ def moe_routing(seed: int, tokens: int, experts: int, topk: int) -> torch.Tensor
     return torch.bincount(ids.to(torch.int64).reshape(-1), minlength=experts)
 
 
-def moe_offsets(counts: torch.Tensor, pad: int = 128) -> tuple[torch.Tensor, torch.Tensor]:
-    """Row offsets [E+1] of expert-sorted rows and scale-row offsets [E+1] padded per expert."""
+def moe_offsets(counts: torch.Tensor) -> torch.Tensor:
+    """Row offsets [E+1] of expert-sorted rows (prefix sums of the counts)."""
     counts = counts.to(torch.int64)
     row = torch.zeros(counts.numel() + 1, dtype=torch.int64)
     row[1:] = torch.cumsum(counts, 0)
-    padded = (counts + pad - 1) // pad * pad
-    sfrow = torch.zeros(counts.numel() + 1, dtype=torch.int64)
-    sfrow[1:] = torch.cumsum(padded, 0)
-    return row, sfrow
+    return row
 
 
 def random_bytes(stream: int, count: int) -> torch.Tensor:

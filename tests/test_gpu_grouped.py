@@ -33,7 +33,7 @@ def _weights(seed, E, n, k):
 def _check(nv, counts, n, k, seed=0, alpha=None, experts_to_check=None):
     counts = torch.as_tensor(counts, dtype=torch.int64)
     E = counts.numel()
-    ro, _ = synth.moe_offsets(counts)
+    ro = synth.moe_offsets(counts)
     t = int(ro[-1])
     xa = synth.activation(seed, t, k)
     qa, sfa = oquant.mxfp4_quantize(xa, ro.numpy())

@@ -121,7 +121,7 @@ def test_mxfp4_quantize_dense_matches_oracle(nv, t, k):
 
 def test_mxfp4_quantize_grouped_matches_oracle(nv):
     counts = torch.tensor([0, 1, 127, 128, 129, 0, 300, 5], dtype=torch.int64)
-    ro, _ = synth.moe_offsets(counts)
+    ro = synth.moe_offsets(counts)
     t, k = int(ro[-1]), 256
     x = synth.activation(21, t, k)
     q, sf = nv.mxfp4_quantize(x.cuda(), row_offsets=ro.cuda())
