@@ -47,16 +47,15 @@ def test_quantiser_sm103_layout(nv, m, k):
     torch.cuda.synchronize()
     # codes do not depend on where the scales go
     assert torch.equal(q0, q1)
-    # SM103 scales = the SM100 scales re-arranged (oracle conversion and the conversion kernel)
-    want = layout.convert_layout(sf0.cpu().numpy(), m, k // 16, to_sm103=True)
-    assert np.array_equal(sf1.cpu().numpy(), want)
+    # both equal the oracle quantiser (bit-exact) in their own layout
+    oq, osf = oquant.nvfp4_quantize(x, gs)
+    assert np.array_equal(q0.cpu().numpy(), oq)
+    assert np.array_equal(sf0.cpu().numpy(), osf)
+    assert np.array_equal(sf1.cpu().numpy(), layout.convert_layout(osf, m, k // 16, to_sm103=True))
+    # and the conversion kernel maps the one onto the other
     conv = nv.sf_convert_layout(sf0, m, k // 16, to_sm103=True)
     torch.cuda.synchronize()
     assert torch.equal(conv, sf1)
-    # and both equal the oracle quantiser (bit-exact) in their own layout
-    oq, osf = oquant.nvfp4_quantize(x, gs)
-    assert np.array_equal(q0.cpu().numpy(), oq)
-    assert np.array_equal(sf1.cpu().numpy(), layout.convert_layout(osf, m, k // 16, to_sm103=True))
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 4096, 7168), (32, 1024, 1024), (100, 256, 2048), (256, 512, 512),
