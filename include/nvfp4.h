@@ -4,9 +4,16 @@
  * Operations (each entry point cites the passage that defines it):
  *   nvfp4_quantize      bf16 -> NVFP4 (packed e2m1 + e4m3 scale per 16, 128x4 swizzled scales)
  *   nvfp4_gemm          D[M,N] = alpha * deq(A) deq(B)^T, bf16 out, fp32 accumulation
+ *                       (+ nvfp4_gemm_plan, nvfp4_gemm_workspace_size, nvfp4_gemm_noalloc)
+ *   nvfp4_quantize_gemm nvfp4_quantize of the activation fused into nvfp4_gemm (M <= 256)
  *   mxfp4_quantize      bf16 -> MXFP4 (packed e2m1 + ue8m0 scale per 32), optionally grouped by expert
  *   mxfp4_grouped_gemm  per-expert D_e = alpha * deq(A_e) deq(B_e)^T for MoE experts
  *   sf_swizzle          row-major scale matrix <-> 128x4 swizzled layout
+ *   nvfp4_sf_convert_layout  128x4 ("SM100") <-> SM103 scale layout
+ *   MoE steps           moe_sort_by_expert, moe_gather_rows, nvfp4_quantize_experts,
+ *                       nvfp4_silu_mul_quantize_experts, nvfp4_grouped_gemm, moe_combine
+ *   sizes and status    nvfp4_sf_bytes, mxfp4_grouped_sf_bytes, moe_sort_workspace_size,
+ *                       nvfp4_check_status, nvfp4_last_error
  *
  * Sources ("page, section"):
  *   [vLLM-SM103]  vLLM fork compare view "add pdl" (sm103 branch)
@@ -16,7 +23,8 @@
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library never
- *     allocates device memory and keeps no pointer after the call returns.
+ *     allocates device memory (nvfp4_gemm_noalloc's scratch is a static array of the library)
+ *     and keeps no pointer after the call returns.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   - Arguments are validated on the host before anything is enqueued.  On error nothing
  *     is launched, the status is returned and nvfp4_last_error() describes it.
