@@ -62,6 +62,12 @@ def test_alpha_and_k_tail(nv):
     _check(nv, [5, 200, 64], 128, 96 * 2, alpha=0.25)
 
 
+def test_largest_expert_count(nv):
+    """1024 experts (the MXFP4 grouped GEMM's limit), most with 0..3 rows."""
+    counts = np.random.default_rng(4).integers(0, 4, 1024).tolist()
+    _check(nv, counts, 64, 64, seed=3)
+
+
 def test_moe_gate_up_sampled_experts(nv):
     """E=128 experts, 4096 tokens top-8 (32768 rows), gate+up N=1536, K=2048; the oracle checks
     the smallest and largest experts and six seeded others."""

@@ -117,8 +117,10 @@ def _expert_weights(E, N, K, seed):
 
 
 @pytest.mark.parametrize("counts,N,K", [([3, 0, 40], 64, 128), ([0, 130, 1, 257], 256, 512),
-                                        (list(np.random.default_rng(2).integers(0, 300, 16)), 1536, 2048)])
+                                        (list(np.random.default_rng(2).integers(0, 300, 16)), 1536, 2048),
+                                        (list(np.random.default_rng(3).integers(0, 4, 512)), 64, 128)])
 def test_nvfp4_grouped_gemm(nv, counts, N, K):
+    """Ragged experts, empty ones, and the largest expert count the NVFP4 grouped GEMM takes (512)."""
     ro = _counts_to_offsets(counts)
     T, E = int(ro[-1]), len(counts)
     x = synth.activation(T + N, T, K, outliers=False)
