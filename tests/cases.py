@@ -20,15 +20,24 @@ def global_scale(x: torch.Tensor) -> np.float32:
     return F32(2688.0) / amax
 
 
+@functools.lru_cache(maxsize=4)
+def _nvfp4_weight(n: int, k: int, seed: int):
+    """B: weight [n,k] N(0,0.02) quantised by the oracle (shared by every M of a shape sweep;
+    callers treat the arrays as read-only)."""
+    xb = synth.weight(seed, n, k)
+    gsb = global_scale(xb)
+    qb, sfb = oquant.nvfp4_quantize(xb, gsb)
+    return xb, gsb, qb, sfb
+
+
 @functools.lru_cache(maxsize=16)
 def nvfp4_operands(m: int, n: int, k: int, seed: int = 0, outliers: bool = True):
     """A: activation [m,k] N(0,1) (+x20 outlier channels), B: weight [n,k] N(0,0.02); both
     quantised to NVFP4 by the oracle with gs = 2688/amax; alpha = 1/(gsA*gsB) in fp32."""
     xa = synth.activation(seed, m, k, outliers=outliers)
-    xb = synth.weight(seed, n, k)
-    gsa, gsb = global_scale(xa), global_scale(xb)
+    xb, gsb, qb, sfb = _nvfp4_weight(n, k, seed)
+    gsa = global_scale(xa)
     qa, sfa = oquant.nvfp4_quantize(xa, gsa)
-    qb, sfb = oquant.nvfp4_quantize(xb, gsb)
     alpha = F32(1.0) / (gsa * gsb)
     return dict(xa=xa, xb=xb, gsa=gsa, gsb=gsb, qa=qa, sfa=sfa, qb=qb, sfb=sfb, alpha=alpha, m=m, n=n, k=k)
 
