@@ -96,7 +96,8 @@ def peaks():
 
 class Clocks:
     """SM clock and clock-event reasons sampled every ~1 ms through NVML (read-only queries)
-    while the timed region runs; nvidia-smi (200 ms) if NVML cannot be loaded."""
+    while the timed region runs.  If NVML cannot be loaded there are no samples: the line's
+    `clocks` then carries null clocks and the reason NVML was unavailable."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 

@@ -215,15 +215,19 @@ nvfp4_status_t nvfp4_quantize_gemm(const void *x, int64_t ldx, const float *gs_x
  * inference engine whose device memory is planned once up front, or code on a latency path where
  * a cudaMalloc would synchronise the device.
  *   Arguments, layouts, alignment and errors are those of nvfp4_gemm.  The call never allocates.
- *   Shapes whose workspace (nvfp4_gemm_workspace_size) exceeds 20 MiB are refused with
- *   NVFP4_ERR_UNSUPPORTED_SHAPE; every plan the selector makes on a GPU of up to 160 SMs fits.
+ *   Shapes whose workspace (nvfp4_gemm_workspace_size) exceeds the array (20 MiB + 4 KiB) are
+ *   refused with NVFP4_ERR_UNSUPPORTED_SHAPE; every plan the selector makes on a GPU of up to
+ *   160 SMs fits (the largest: 80 split tiles on 160 CTAs, 20 MiB + 512 bytes).
  *   The array is shared by every call on the device: calls that may overlap (other streams,
  *   other threads) race on it and must not use this entry point concurrently.
- *   The array's address is looked up on the first call on each device (cudaGetSymbolAddress);
- *   a caller that records work for later replay should make one call before it starts recording.
+ *   The array's address is looked up (cudaGetSymbolAddress) on the first call on each device,
+ *   and again on the first call after the device got a new context (a device reset); a caller
+ *   that records work for later replay should make one call before it starts recording.
  *   The arrival counters must read zero when the kernel starts: before each launch of a split
- *   plan this entry point clears them with cudaMemsetAsync on `stream` (so a call after one
- *   that timed out starts clean); the partial-tile slots need no initialisation. */
+ *   plan this entry point enqueues a one-CTA kernel on `stream` that clears them (so a call
+ *   after one that timed out starts clean); the partial-tile slots need no initialisation.
+ *   That kernel takes the call's NVFP4_FLAG_PDL too: it waits for the preceding kernel before
+ *   clearing, while the GEMM starts beside it and streams its weight as nvfp4_gemm would. */
 nvfp4_status_t nvfp4_gemm_noalloc(const uint8_t *a, const uint8_t *sfa, const uint8_t *b, const uint8_t *sfb,
                                   const float *alpha, void *d, int64_t m, int64_t n, int64_t k,
                                   uint32_t flags, nvfp4_stream_t stream);

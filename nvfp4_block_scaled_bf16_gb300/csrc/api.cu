@@ -19,13 +19,18 @@ thread_local char t_msg[512] = "";
 
 constexpr int kMaxDevices = 64;
 struct DevState {
-  std::atomic<bool> ready{false};  // set (release) after the fields below are filled in
+  // context the fields below were filled in for (0: not yet); set (release) after them
+  std::atomic<unsigned long long> ctx{0};
   bool ok = false;
   DeviceInfo info{};
   char why[200] = "";
 };
 DevState g_dev[kMaxDevices];
 std::mutex g_mu;
+
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_once;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -34,6 +39,7 @@ cudaError_t g_encode_err = cudaSuccess;
 struct SmemEntry {
   const void *fn;
   int device;
+  unsigned long long ctx;  // the attribute belongs to the context it was set in
   int bytes;
 };
 SmemEntry g_smem[256];
@@ -50,15 +56,42 @@ nvfp4_status_t fail(nvfp4_status_t code, const char *fmt, ...) {
 
 void clear_error() { t_msg[0] = '\0'; }
 
+unsigned long long current_context_id() {
+  std::call_once(g_ctx_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!g_ctx_current || !g_ctx_id || g_ctx_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      g_ctx_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 nvfp4_status_t current_device(DeviceInfo *out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
   DevState &st = g_dev[dev];
-  if (!st.ready.load(std::memory_order_acquire)) {
+  // The status word's address belongs to the context it was looked up in: after a device reset
+  // (a new primary context) the module is loaded again, possibly elsewhere, so the cached
+  // address is looked up again.  cudaGetDevice above has made the context current.
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || st.ctx.load(std::memory_order_acquire) != ctx) {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!st.ready.load(std::memory_order_relaxed)) {
+    if (ctx == 0 || st.ctx.load(std::memory_order_relaxed) != ctx) {
+      st.ok = false;
+      st.why[0] = '\0';
       int major = 0, minor = 0, sms = 0;
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
@@ -78,7 +111,10 @@ nvfp4_status_t current_device(DeviceInfo *out) {
         st.info.sm_count = sms;
         st.info.status = static_cast<unsigned int *>(status);
       }
-      st.ready.store(true, std::memory_order_release);
+      st.ctx.store(ctx, std::memory_order_release);
+      if (!st.ok) return fail(NVFP4_ERR_UNSUPPORTED_DEVICE, "%s", st.why);
+      *out = st.info;
+      return NVFP4_OK;
     }
   }
   if (!st.ok) return fail(NVFP4_ERR_UNSUPPORTED_DEVICE, "%s", st.why);
@@ -143,10 +179,11 @@ nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_
 }
 
 nvfp4_status_t allow_smem(const void *fn, int bytes, int device) {
-  {
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0) {
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < g_smem_n; ++i)
-      if (g_smem[i].fn == fn && g_smem[i].device == device && g_smem[i].bytes >= bytes)
+      if (g_smem[i].fn == fn && g_smem[i].device == device && g_smem[i].ctx == ctx && g_smem[i].bytes >= bytes)
         return NVFP4_OK;
   }
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -155,7 +192,12 @@ nvfp4_status_t allow_smem(const void *fn, int bytes, int device) {
     return fail(NVFP4_ERR_CUDA, "cudaFuncSetAttribute(smem=%d): %s", bytes, cudaGetErrorString(e));
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_smem_n < 256) g_smem[g_smem_n++] = SmemEntry{fn, device, bytes};
+  for (int i = 0; i < g_smem_n; ++i)
+    if (g_smem[i].fn == fn && g_smem[i].device == device) {  // a newer context or a larger size
+      g_smem[i] = SmemEntry{fn, device, ctx, bytes};
+      return NVFP4_OK;
+    }
+  if (g_smem_n < 256) g_smem[g_smem_n++] = SmemEntry{fn, device, ctx, bytes};
   return NVFP4_OK;
 }
 

@@ -105,9 +105,8 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     pl.sk_tiles = 0;
     pl.ctas = tiles < sm_count ? tiles : sm_count;
   }
-  if (pl.sk_tiles > 0)
-    pl.ws_bytes = round_up(static_cast<int64_t>(pl.sk_tiles) * 4, kWsAlign) +
-                  static_cast<size_t>(pl.ctas) * 2 * 128 * pl.bn * 4;
+  // (stream-K plans use 128-wide tiles and at most sm_count / 2 split tiles)
+  if (pl.sk_tiles > 0) pl.ws_bytes = stream_k_workspace_bytes(pl.sk_tiles, pl.ctas, pl.bn);
   // Rings as deep as shared memory allows: a swap-AB CTA then has its whole K run in flight
   // from the start (the decode GEMM is bound by load latency, not by shared memory).  The
   // narrowest tiles instead keep a 4-stage ring so that two CTAs fit an SM: under PDL the next

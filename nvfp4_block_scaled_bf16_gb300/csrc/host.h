@@ -21,8 +21,18 @@ struct DeviceInfo {
   int sm_count;
   unsigned int *status;  // device status word (address of a __device__ variable)
 };
-// Checks that the current device is sm_103 and returns its cached properties.
+// Checks that the current device is sm_103 and returns its properties, cached per device for
+// as long as its context lives (a device reset makes a new context: they are looked up again).
 nvfp4_status_t current_device(DeviceInfo *out);
+
+// Unique id of the calling thread's current CUDA context (cuCtxGetId); 0 if there is none.
+unsigned long long current_context_id();
+
+// Bytes of the stream-K workspace: one arrival counter per split tile (rounded up to 256 bytes),
+// then two fp32 partial-tile slots of 128 x bn per CTA.
+constexpr size_t stream_k_workspace_bytes(int sk_tiles, int ctas, int bn) {
+  return (static_cast<size_t>(sk_tiles) * 4 + 255) / 256 * 256 + static_cast<size_t>(ctas) * 2 * 128 * bn * 4;
+}
 
 // Wait limit (SM clock cycles) for the bounded pipeline waits.
 long long wait_limit(uint32_t flags);

@@ -46,14 +46,6 @@ def nvfp4_gemm(a, sfa, b, sfb, alpha, m: int, n: int, k: int) -> np.ndarray:
     return np.float64(np.float32(alpha)) * (A @ B.T)
 
 
-def nvfp4_gemm_rows(a, sfa, b, sfb, alpha, m: int, n: int, k: int, rows) -> np.ndarray:
-    """Rows ``rows`` of R only (for spot checks at sizes where the full product is slow)."""
-    rows = np.asarray(rows, dtype=np.int64)
-    A = dequantize(a, sfa, m, k, 16, "e4m3")[rows]
-    B = dequantize(b, sfb, n, k, 16, "e4m3")
-    return np.float64(np.float32(alpha)) * (A @ B.T)
-
-
 def abs_product_sum(A: np.ndarray, B: np.ndarray, alpha) -> np.ndarray:
     """sum_k |alpha * a(m,k) * b(n,k)| for dequantised operands."""
     return abs(np.float64(np.float32(alpha))) * (np.abs(A) @ np.abs(B).T)

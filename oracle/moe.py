@@ -109,11 +109,6 @@ def sort_by_expert(topk_ids, num_experts: int):
     return row_offsets, src, pos.reshape(T, topk)
 
 
-def gather_rows(x, src) -> np.ndarray:
-    """Permuted activation: row r = x[src[r]]."""
-    return np.asarray(x)[np.asarray(src, dtype=np.int64)]
-
-
 def nvfp4_quantize_experts(x, row_offsets, gs) -> tuple[np.ndarray, np.ndarray]:
     """bf16 [T, K] rows grouped by expert -> (packed e2m1 [T, K/2], grouped e4m3 scales).
     Expert e's rows use global scale gs[e]; its scales form their own 128-row block starting at

@@ -164,3 +164,34 @@ def test_grouped_equals_per_expert_dense():
         cb, scb = quant.mxfp4_block_codes(xb[e])
         B = formats.e2m1_decode(cb) * np.repeat(formats.ue8m0_decode(scb), 32, axis=1)
         assert np.array_equal(out[e][2], A[ro[e]:ro[e + 1]] @ B.T)
+
+
+def test_dequantize_matches_exact_rationals():
+    """deq(q, sf)[r, k] = e2m1(nibble) * e4m3(scale of block k/16), decoded through the spec
+    table and torch's e4m3 cast with the row-major scale matrix (not the oracle's decoders)."""
+    rows, k = 5, 64
+    q, sf, sc = _random_operands(9, rows, k)
+    got = gemm.dequantize(q, sf, rows, k, 16, "e4m3")
+    e2 = _e2m1_table()
+    e4 = torch.from_numpy(sc).view(torch.float8_e4m3fn).double().numpy()
+    for r in range(rows):
+        for kk in range(k):
+            byte = int(q[r, kk // 2])
+            nib = byte & 0xF if kk % 2 == 0 else byte >> 4
+            assert Fraction(float(got[r, kk])) == e2[nib] * Fraction(float(e4[r, kk // 16])), (r, kk)
+
+
+def test_abs_product_sum_and_tolerance_by_hand():
+    """sum_k |alpha a b| by explicit loops in exact rationals, and the acceptance bound on
+    hand-worked values: ulp_bf16(3) = 2^-6, so |R| = 3 with abs-sum 100 allows 2^-6 + 1e-3."""
+    rng = np.random.default_rng(5)
+    A = rng.normal(size=(3, 7))
+    B = rng.normal(size=(4, 7))
+    alpha = -0.625
+    got = gemm.abs_product_sum(A, B, alpha)
+    for i in range(3):
+        for j in range(4):
+            s = sum(abs(Fraction(alpha) * Fraction(A[i, kk]) * Fraction(B[j, kk])) for kk in range(7))
+            assert abs(Fraction(float(got[i, j])) - s) <= Fraction(1, 10 ** 12) * s
+    tol = gemm.tolerance(np.array([3.0, -3.0, 0.0, 1.0]), np.array([100.0, 100.0, 0.0, 0.0]))
+    assert np.array_equal(tol, np.array([2.0 ** -6 + 1e-3, 2.0 ** -6 + 1e-3, 0.0, 2.0 ** -7]))

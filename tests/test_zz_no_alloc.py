@@ -43,8 +43,35 @@ def test_two_calls_match_the_workspace_entry_point(nv, m, n, k, split):
         assert_within(d1, R, tol, f"no-alloc {m}x{n}x{k}")
 
 
+def test_dirty_counters_leave_split_tiles_unwritten(nv):
+    """What the counter clearing guards against, shown on nvfp4_gemm with a caller workspace:
+    arrival counters that do not start at zero (as a split call that timed out part way can
+    leave them) make no CTA the last of its tile, so the split tiles are never written and the
+    counters stay set.  nvfp4_gemm_noalloc clears its counters before every split launch."""
+    m, n, k = 512, 512, 16384
+    plan = nv.nvfp4_gemm_plan(m, n, k)
+    assert plan["sk_tiles"] > 0 and plan["dp_tiles"] == 0
+    ops = nvfp4_operands(m, n, k, seed=24)
+    args = _args(ops)
+    ws = nv.gemm_workspace(nv.gemm_workspace_size(m, n, k))
+    counters = ws[:4 * plan["sk_tiles"]].view(torch.int32)
+    counters.fill_(1000)                       # no arrival can see n - 1
+    d = torch.full((m, n), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nv.nvfp4_gemm(*args, d=d, workspace=ws)
+    torch.cuda.synchronize()
+    nv.check_status()
+    assert torch.isnan(d.float()).all()        # no split tile was finished
+    assert (counters > 1000).all()             # and the counters are still set
+    good = nv.nvfp4_gemm_noalloc(*args)
+    torch.cuda.synchronize()
+    nv.check_status()
+    R, tol = reference(ops)
+    assert_within(good, R, tol, "no-alloc beside a dirty workspace")
+
+
 def test_call_after_a_timeout_starts_clean(nv):
-    """A timed-out split call may leave arrival counters set; the next call clears them first."""
+    """A split call that times out (every CTA here gives up at its first stage); the next call
+    on the static scratch must give the oracle's result."""
     m, n, k = 512, 512, 16384
     ops = nvfp4_operands(m, n, k, seed=22)
     args = _args(ops)
@@ -60,7 +87,7 @@ def test_call_after_a_timeout_starts_clean(nv):
     assert_within(d, R, tol, "no-alloc after time-out")
 
 
-def test_refuses_what_nvfp4_gemm_refuses_without_enqueueing(nv):
+def test_refuses_what_nvfp4_gemm_refuses(nv):
     ops = nvfp4_operands(300, 1024, 16384, seed=23)
     a, sfa, b, sfb, al = _args(ops)
     with pytest.raises(nv.NVFP4Error) as e:
