@@ -52,6 +52,10 @@ DECODE_MS = (1, 4, 8, 16, 32, 64, 128, 256)
 PREFILL = ((1024, 4096, 7168), (2048, 4096, 7168), (4096, 4096, 7168), (4096, 4096, 4096), (128, 7168, 2048))
 # FlashInfer PR 4865 B300 table (best of its SM100/SM103 kernels, ms), N=4096 K=7168: context only
 PAGES_B300_DECODE_MS = {1: 0.0100, 4: 0.0099, 8: 0.0096, 16: 0.0097, 32: 0.0097, 64: 0.0094, 128: 0.0096, 256: 0.0091}
+# same table, other shapes (us, faster of the two kernels): context only
+PAGES_B300_PREFILL_US = {(1024, 4096, 7168): 13.4, (2048, 4096, 7168): 21.5, (4096, 4096, 7168): 36.7,
+                         (4096, 4096, 4096): 25.1, (128, 7168, 2048): 6.1, (256, 14336, 4096): 12.6,
+                         (512, 14336, 4096): 17.4}
 
 
 def gemm_bytes(m, n, k):
@@ -535,6 +539,152 @@ def timed_replays(g, n: int, flush: L2Flush, before=None, after=None) -> list[fl
     return out
 
 
+# ---------------------------------------------------------------------------- per-config lines
+# Every graded configuration on its own (the metric is "... vs M"): per GEMM, CUDA-event time
+# with cold L2, throughput, and the fraction of the binding roofline
+#   t_roof = max(flops / FP4 peak, algorithmic bytes / HBM peak),  frac = t_roof / t.
+# "us_per_gemm": a PDL chain of R GEMMs of the shape with R distinct weight copies (the
+# steady state of back-to-back layers), time / R; "single_us": one GEMM per graph replay
+# (includes the graph's launch gap on the device, ~1-2 us, so it understates short kernels).
+PER_CONFIG_REPS = 20
+
+
+def _graph_ms(fns, flush, reps=PER_CONFIG_REPS, warm=3) -> float:
+    g = capture(fns)
+    for _ in range(warm):
+        g.replay()
+    torch.cuda.synchronize()
+    t = statistics.mean(timed_replays(g, reps, flush))
+    del g
+    return t
+
+
+def _qweight(nv, seed, n, k, dev="cuda"):
+    w = synth.weight(seed, n, k, device=dev)
+    gsw = _gs(w)
+    qb, sfb = nv.nvfp4_quantize(w, torch.tensor([gsw], device=dev))
+    del w
+    return qb, sfb, gsw
+
+
+def _qact(nv, seed, m, k, gsw, dev="cuda"):
+    x = synth.activation(seed, m, k, device=dev)
+    gsa = _gs(x)
+    qa, sfa = nv.nvfp4_quantize(x, torch.tensor([gsa], device=dev))
+    al = torch.tensor([float(np.float32(1.0) / (np.float32(gsa) * np.float32(gsw)))], device=dev)
+    return x, gsa, qa, sfa, al
+
+
+def _entry(kind, m, n, k, us, flops, nbytes, hbm, fp4, **extra):
+    t = us * 1e-6
+    t_hbm, t_fp4 = nbytes / (hbm * 1e9), flops / (fp4 * 1e12)
+    e = {"config": kind, "m": m, "n": n, "k": k, "us_per_gemm": round(us, 3),
+         "tflops": round(flops / t / 1e12, 1), "gbs": round(nbytes / t / 1e9, 1),
+         "bound": "hbm" if t_hbm >= t_fp4 else "tensor", "roof_us": round(max(t_hbm, t_fp4) * 1e6, 3),
+         "frac": round(max(t_hbm, t_fp4) / t, 4)}
+    e.update(extra)
+    return e
+
+
+def per_config(nv, flush, hbm, fp4):
+    P = nv.FLAG_PDL
+    out = []
+
+    def gemm_chain(shape, copies, seed):
+        m, n, k = shape
+        ws = nv.gemm_workspace(nv.gemm_workspace_size(m, n, k))
+        qb, sfb, gsw = _qweight(nv, seed, n, k)
+        ws_ = [(qb, sfb)] + [(qb.clone(), sfb.clone()) for _ in range(copies - 1)]
+        _, _, qa, sfa, al = _qact(nv, seed + 100, m, k, gsw)
+        d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        fns = [(lambda b=b, sb=sb: nv.nvfp4_gemm(qa, sfa, b, sb, al, d, flags=P, workspace=ws)) for b, sb in ws_]
+        chain = _graph_ms(fns, flush) * 1e3 / copies
+        single = _graph_ms(fns[:1], flush) * 1e3
+        return chain, single
+
+    for m in DECODE_MS:
+        n, k = 4096, 7168
+        chain, single = gemm_chain((m, n, k), 8, 0)
+        out.append(_entry("decode", m, n, k, chain, 2.0 * m * n * k, gemm_bytes(m, n, k), hbm, fp4,
+                          single_us=round(single, 3), chain=8,
+                          pages_b300_us=round(PAGES_B300_DECODE_MS[m] * 1e3, 2)))
+    for (m, n, k) in PREFILL:
+        chain, single = gemm_chain((m, n, k), 2, 1)
+        out.append(_entry("prefill", m, n, k, chain, 2.0 * m * n * k, gemm_bytes(m, n, k), hbm, fp4,
+                          single_us=round(single, 3), chain=2,
+                          pages_b300_us=PAGES_B300_PREFILL_US.get((m, n, k))))
+    # quantiser -> GEMM, with and without programmatic dependent launch (4 pairs, own weights)
+    for m in (256, 512):
+        n, k = 14336, 4096
+        qb, sfb, gsw = _qweight(nv, 2, n, k)
+        wts = [(qb, sfb)] + [(qb.clone(), sfb.clone()) for _ in range(3)]
+        res = {}
+        for tag, fl in (("pdl", P), ("no_pdl", 0)):
+            fns, gfns = [], []
+            for i, (b, sb) in enumerate(wts):
+                x, gsa, qa, sfa, al = _qact(nv, 200 + i, m, k, gsw)
+                gs_d = torch.tensor([gsa], dtype=torch.float32, device="cuda")
+                d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+                fns.append(lambda x=x, g=gs_d, q=qa, s_=sfa, fl=fl: nv.nvfp4_quantize(x, g, q, s_, flags=fl))
+                g = (lambda q=qa, s_=sfa, b=b, sb=sb, al=al, d=d, fl=fl: nv.nvfp4_gemm(q, s_, b, sb, al, d, flags=fl))
+                fns.append(g)
+                gfns.append(g)
+            res[tag] = _graph_ms(fns, flush) * 1e3 / len(wts)
+            if tag == "pdl":
+                res["gemm"] = _graph_ms(gfns, flush) * 1e3 / len(wts)
+        out.append(_entry("e2e_gemm", m, n, k, res["gemm"], 2.0 * m * n * k, gemm_bytes(m, n, k), hbm, fp4,
+                          quant_gemm_pdl_us=round(res["pdl"], 3), quant_gemm_no_pdl_us=round(res["no_pdl"], 3),
+                          pdl_speedup=round(res["no_pdl"] / res["pdl"], 3), chain=len(wts),
+                          pages_b300_us=PAGES_B300_PREFILL_US.get((m, n, k))))
+        del wts, qb, sfb
+    # MoE grouped GEMMs: 128 experts, 4096 tokens top-8; MXFP4 and NVFP4 formats
+    E, T, topk, H, I = 128, 4096, 8, 2048, 768
+    counts = synth.moe_routing(0, T, E, topk)
+    ro = synth.moe_offsets(counts).cuda()
+    rows = int(counts.sum())
+    for fmt in ("mxfp4", "nvfp4"):
+        for name, n, k, seed in (("gate_up", 2 * I, H, 1), ("down", H, I, 2)):
+            wb = synth.weight(seed, n, k, experts=E, device="cuda")
+            x = synth.activation(seed + 10, rows, k, outliers=False, device="cuda")
+            d = torch.empty((rows, n), dtype=torch.bfloat16, device="cuda")
+            if fmt == "mxfp4":
+                qb = torch.empty((E, n, k // 2), dtype=torch.uint8, device="cuda")
+                sfb = torch.empty((E, nv.sf_bytes(n, k, 32)), dtype=torch.uint8, device="cuda")
+                for e in range(E):
+                    nv.mxfp4_quantize(wb[e], q=qb[e], sf=sfb[e])
+                qa, sfa = nv.mxfp4_quantize(x, ro)
+                fn = (lambda: nv.mxfp4_grouped_gemm(qa, sfa, ro, qb, sfb, None, d, flags=P))
+                nbytes = grouped_bytes(E, rows, n, k)
+            else:
+                qb = torch.empty((E, n, k // 2), dtype=torch.uint8, device="cuda")
+                sfb = torch.empty((E, nv.sf_bytes(n, k, 16)), dtype=torch.uint8, device="cuda")
+                gsb = torch.empty(E, dtype=torch.float32)
+                for e in range(E):
+                    gsb[e] = _gs(wb[e])
+                    nv.nvfp4_quantize(wb[e], gsb[e:e + 1].cuda(), q=qb[e], sf=sfb[e])
+                gsa = _gs(x)
+                qa, sfa = nv.nvfp4_quantize_experts(x, ro, torch.full((E,), gsa, device="cuda"))
+                al = (1.0 / (gsa * gsb)).to(torch.float32).cuda()
+                fn = (lambda: nv.nvfp4_grouped_gemm(qa, sfa, ro, qb, sfb, al, d, flags=P))
+                nbytes = nvfp4_grouped_bytes(E, rows, n, k)
+            del wb, x
+            us = _graph_ms([fn], flush) * 1e3
+            out.append(_entry(f"moe_{fmt}_{name}", rows, n, k, us, 2.0 * rows * n * k, nbytes, hbm, fp4,
+                              experts=E, expert_rows_min=int(counts.min()), expert_rows_max=int(counts.max())))
+            del qb, sfb, qa, sfa, d
+    torch.cuda.empty_cache()
+    return out
+
+
+def targets(per):
+    """The two throughput targets, read off the per-config entries."""
+    dec = [e for e in per if e["config"] == "decode" and e["m"] <= 32]
+    pre = [e for e in per if e["config"] == "prefill" and e["m"] >= 2048]
+    return {"decode_m_le_32_hbm_frac_min": min(e["frac"] for e in dec) if dec else None,
+            "prefill_m_ge_2048_fp4_frac_min": min(e["frac"] for e in pre) if pre else None,
+            "target": 0.70}
+
+
 def barrier(dist_on: bool, device: str = "cuda"):
     if dist_on:
         torch.distributed.barrier()
@@ -688,6 +838,14 @@ def run_ours(args, dist_on, rank, world):
             row["pdl_speedup"] = round(row["no_pdl_us"] / row["pdl_us"], 3)
             per_m[str(m)] = row
         line["pipeline"] = per_m
+    if args.per_config and wl.name == "decode":
+        per = per_config(nv, flush, hbm, fp4_peak_tflops)
+        line["per_config"] = per
+        line["targets"] = targets(per)
+        line["per_config_method"] = (
+            "CUDA events, L2 flushed before every replay; us_per_gemm = PDL chain of `chain` GEMMs with "
+            "distinct weight copies / chain; single_us = one GEMM per replay; frac = max(flops/FP4 peak, "
+            "bytes/HBM peak) / time with the measured peaks (FP4 = bf16 burst x 6)")
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline(args.workload)
         print(json.dumps(line), flush=True)
@@ -778,6 +936,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(MAKERS), default="decode")
     ap.add_argument("--shapes", default="", help="custom quant->GEMM chain, e.g. '32,4096,7168;1024,4096,7168'")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg (profiling runs)")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the per-configuration lines (decode, prefill, e2e, MoE GEMMs one by one)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3   # at least three untimed warm-up steps

@@ -20,6 +20,10 @@ Recipe (stated once, used everywhere):
   picked by a partial Fisher-Yates shuffle driven by stream ``seed*8+2`` and
   multiplied by 20 before the rounding to bf16 (the "0.1% of channels scaled
   x20" of the decode and prefill workloads).
+* Every generator takes an optional ``device``: the same steps then run there.  On a GPU the
+  fp64 log / cos / sin may differ from the host's in the last bit, so a value can, rarely, round
+  to a neighbouring bf16; the parity tests therefore draw on the host, and the benchmark draws
+  its large timing inputs on the GPU.
 * MoE routing: fp32 logits N(0,1) of shape [tokens, experts] from stream
   ``seed*8+3``, softmax over experts in fp32, top-k by a stable descending sort
   (ties go to the lower expert id); the per-expert row counts are what the
@@ -58,9 +62,9 @@ def _mix64(z: torch.Tensor) -> torch.Tensor:
     return z ^ _lsr(z, 31)
 
 
-def splitmix64(stream: int, start: int, count: int) -> torch.Tensor:
+def splitmix64(stream: int, start: int, count: int, device=None) -> torch.Tensor:
     """Outputs ``start .. start+count-1`` of SplitMix64 stream ``stream`` as int64 bit patterns."""
-    idx = torch.arange(start + 1, start + count + 1, dtype=torch.int64)
+    idx = torch.arange(start + 1, start + count + 1, dtype=torch.int64, device=device)
     state = idx * _s64(GOLDEN) + _s64(stream)
     return _mix64(state)
 
@@ -77,14 +81,14 @@ def splitmix64_py(stream: int, count: int) -> list[int]:
     return out
 
 
-def normal(stream: int, count: int) -> torch.Tensor:
+def normal(stream: int, count: int, device=None) -> torch.Tensor:
     """``count`` standard normals (fp64) from SplitMix64 stream ``stream`` by Box-Muller."""
-    out = torch.empty(count, dtype=torch.float64)
+    out = torch.empty(count, dtype=torch.float64, device=device)
     pairs = (count + 1) // 2
     done = 0
     while done < pairs:
         n = min(_CHUNK, pairs - done)
-        r = splitmix64(stream, 2 * done, 2 * n).view(n, 2)
+        r = splitmix64(stream, 2 * done, 2 * n, device).view(n, 2)
         u1 = (_lsr(r[:, 0], 11) + 1).to(torch.float64) * 2.0 ** -53
         u2 = _lsr(r[:, 1], 11).to(torch.float64) * 2.0 ** -53
         rad = torch.sqrt(-2.0 * torch.log(u1))
@@ -114,19 +118,19 @@ def outlier_channels(seed: int, k: int) -> torch.Tensor:
     return torch.tensor(sorted(perm[:count]), dtype=torch.int64)
 
 
-def activation(seed: int, m: int, k: int, outliers: bool = True, std: float = 1.0) -> torch.Tensor:
+def activation(seed: int, m: int, k: int, outliers: bool = True, std: float = 1.0, device=None) -> torch.Tensor:
     """bf16 activation [m, k]: N(0, std^2) with optional x20 outlier channels."""
-    v = normal(seed * 8 + STREAM_ACT, m * k).view(m, k) * std
+    v = normal(seed * 8 + STREAM_ACT, m * k, device).view(m, k) * std
     if outliers and m > 0:
-        v[:, outlier_channels(seed, k)] *= 20.0
+        v[:, outlier_channels(seed, k).to(v.device)] *= 20.0
     return to_bf16(v)
 
 
-def weight(seed: int, n: int, k: int, std: float = 0.02, experts: int | None = None) -> torch.Tensor:
+def weight(seed: int, n: int, k: int, std: float = 0.02, experts: int | None = None, device=None) -> torch.Tensor:
     """bf16 weight [n, k] (or [experts, n, k]) drawn N(0, std^2)."""
     shape = (n, k) if experts is None else (experts, n, k)
     count = math.prod(shape)
-    return to_bf16(normal(seed * 8 + STREAM_WEIGHT, count).view(shape) * std)
+    return to_bf16(normal(seed * 8 + STREAM_WEIGHT, count, device).view(shape) * std)
 
 
 def moe_topk(seed: int, tokens: int, experts: int, topk: int) -> tuple[torch.Tensor, torch.Tensor]:
