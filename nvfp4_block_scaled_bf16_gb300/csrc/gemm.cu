@@ -3,7 +3,8 @@
 // Selector (the role of "SM103 Dispatch" in vLLM fork compare view "add pdl",
 // nvfp4_scaled_mm_kernels.cu, which buckets M into [1,16], (16,256], (256,inf); and of the
 // narrow output tiles FlashInfer PR 4865's "Reviewer Notes" credit for small-M speed):
-//   M <= 256  swap A and B: the weight's rows fill the 128-row MMA slot and the tokens the
+//   M <= 256  (unless CTA-pair tiles fit, below) swap A and B: the weight's rows fill the
+//             128-row MMA slot and the tokens the
 //             N slot (N = 32, 64, 128 or 256, the smallest that holds M), so no MMA row is
 //             wasted on padding; K is split over a thread-block cluster of up to 8 CTAs until the
 //             grid covers the SMs (both CTA slots of each SM for N = 32), and the partial tiles
@@ -17,8 +18,9 @@
 //             CTA are in flight: with cold HBM, requesting every stage at once made all of them
 //             land together, leaving no load for the MMAs to overlap.
 //   M >  256  256 x 256 tiles computed by CTA pairs (cta_group::2) when N is a multiple of 256
-//             and there are at least as many 128 x 256 tiles as SMs; otherwise 128 x 128 tiles on
-//             single CTAs.  Persistent over the SMs, double-buffered accumulators where tensor
+//             and either there are at least as many 128 x 256 tiles as SMs, or M > 128 and the
+//             pair tiles occupy at least a quarter of the pairs; otherwise 128 x 128 tiles on
+//             single CTAs.  A pair's ring stage holds two 256-wide K steps when K % 256 == 0.  Persistent over the SMs, double-buffered accumulators where tensor
 //             memory allows (128 x 128).  When the tiles fill less than half the SMs and K is
 //             long (>= 4 K stages per SM), the (tile, K stage) units are split stream-K over all
 //             SMs and split tiles are added up through the workspace.  Splitting the last wave of
@@ -34,6 +36,7 @@ struct Plan {
   int swap, bn, splits, stages, ctas, m_tiles, n_tiles, k_tiles, dp_tiles, sk_tiles;
   int pair;  // 1: 256 x 256 tiles computed by CTA pairs (cta_group::2); m_tiles counts 256 rows
   int resident, nst_max, lookahead;  // see GemmArgs
+  int ks;    // 256-wide K steps per ring stage (2: pairs whose K is a multiple of 256)
   size_t ws_bytes;
 };
 
@@ -55,9 +58,14 @@ int max_contributors(int64_t sk_tiles, int k_tiles, int ctas) {
 
 Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   Plan pl{};
+  pl.ks = 1;
   pl.k_tiles = static_cast<int>(ceil_div(k, 256));
   pl.splits = 1;
-  if (m <= 256) {
+  // 256 x 256 tiles on CTA pairs pay from 129 tokens on when they occupy at least a quarter of
+  // the pairs (measured, cold PDL chains: 256 x 14336 x 4096 23.0 -> 16.0 us, 1024 x 4096 x 7168
+  // 31.0 -> 23.8 us; with fewer tiles, e.g. 256 x 4096 x 7168, swap-AB split-K stays faster)
+  const bool pair_tiles = n % 256 == 0 && m > 128 && ceil_div(m, 256) * (n / 256) >= sm_count / 4;
+  if (m <= 256 && !pair_tiles) {
     pl.swap = 1;
     pl.bn = m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
     pl.m_tiles = static_cast<int>(ceil_div(n, 128));  // weight rows
@@ -77,11 +85,16 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     pl.ctas = tiles * s;
   } else {
     pl.swap = 0;
-    pl.bn = (n % 256 == 0 && ceil_div(m, 128) * (n / 256) >= sm_count) ? 256 : 128;
+    pl.bn = (pair_tiles || (n % 256 == 0 && ceil_div(m, 128) * (n / 256) >= sm_count)) ? 256 : 128;
     // 256-wide tiles go to CTA pairs: a single CTA's 128 x 256 tile moves 54 KB through shared
     // memory per K stage (TMA writes, MMA reads, scale reads) and is bound by that bandwidth; a
     // pair stages half of B per CTA.
     pl.pair = pl.bn == 256 ? 1 : 0;
+    // a pair lands two K steps of each operand with one 3-D copy when K allows the stage view
+    if (pl.pair && k % 256 == 0) {
+      pl.ks = 2;
+      pl.k_tiles = static_cast<int>(ceil_div(k, 512));
+    }
     pl.m_tiles = static_cast<int>(ceil_div(m, pl.pair ? 256 : 128));
     pl.n_tiles = static_cast<int>(ceil_div(n, pl.bn));
     const int tiles = pl.m_tiles * pl.n_tiles;
@@ -116,7 +129,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     case 32: pl.stages = 4; break;
     case 64: pl.stages = 7; break;
     case 128: pl.stages = 6; break;
-    default: pl.stages = pl.pair ? 6 : 4; break;
+    default: pl.stages = pl.pair ? (pl.ks == 2 ? 3 : 6) : 4; break;
   }
   // A swap-AB CTA holds one tile; when its whole K slice fits the ring (and K is a whole number of
   // 256-wide stages), the activation and both scale slices land with one copy each.
@@ -148,7 +161,8 @@ nvfp4_status_t with_config(const Plan &pl, F &&f) {
     case 64: return f(GemmCfg<64, 7, false, false>{});
     case 128: return pl.swap ? f(GemmCfg<128, 6, false, false>{}) : f(GemmCfg<128, 6, false, true>{});
     default:
-      return pl.swap ? f(GemmCfg<256, 4, false, false>{}) : f(GemmCfg<256, 6, false, true, 1, true>{});
+      if (pl.swap) return f(GemmCfg<256, 4, false, false>{});
+      return pl.ks == 2 ? f(GemmCfg<256, 3, false, true, 1, true, 1024, 2>{}) : f(GemmCfg<256, 6, false, true, 1, true>{});
   }
 }
 
@@ -238,20 +252,20 @@ nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, 
   const uint8_t *sfopa = pl.swap ? sfb : sfa, *sfopb = pl.swap ? sfa : sfb;
   const int64_t rows_a = pl.swap ? n : m, rows_b = pl.swap ? m : n;
   CUtensorMap ta, tb, tb3;
-  st = encode_tmap_2d_u8(&ta, opa, k / 2, rows_a, k / 2, 128, 128, true);
-  if (st != NVFP4_OK) return st;
-  if (fused) {
-    tb = ta;  // operand B is produced in the kernel: its maps are unused
-  } else {
-    st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.pair ? pl.bn / 2 : pl.bn, true);
-    if (st != NVFP4_OK) return st;
-  }
-  if (pl.resident && !fused) {
-    st = encode_tmap_stages_u8(&tb3, opb, k / 2, rows_b, pl.bn, pl.nst_max);
-    if (st != NVFP4_OK) return st;
-  } else {
+  if (pl.ks == 2) {
+    // stage views: a box is two 256-wide K steps (two 128-byte rows) of 128 rows
+    st = encode_tmap_stages_u8(&ta, opa, k / 2, rows_a, 128, 2);
+    if (st == NVFP4_OK) st = encode_tmap_stages_u8(&tb, opb, k / 2, rows_b, pl.bn / 2, 2);
     tb3 = tb;  // unused
+  } else {
+    st = encode_tmap_2d_u8(&ta, opa, k / 2, rows_a, k / 2, 128, 128, true);
+    if (st == NVFP4_OK && fused) tb = ta;  // operand B is produced in the kernel: its maps are unused
+    else if (st == NVFP4_OK)
+      st = encode_tmap_2d_u8(&tb, opb, k / 2, rows_b, k / 2, 128, pl.pair ? pl.bn / 2 : pl.bn, true);
+    if (st == NVFP4_OK && pl.resident && !fused) st = encode_tmap_stages_u8(&tb3, opb, k / 2, rows_b, pl.bn, pl.nst_max);
+    else tb3 = tb;  // unused
   }
+  if (st != NVFP4_OK) return st;
 
   GemmArgs args{};
   args.sfa = sfopa;

@@ -75,7 +75,7 @@ enum : int {
 };
 
 template <int BN_, int STAGES_, bool MX_, bool MULTI_TILE_ = true, int MIN_BLOCKS_ = 1, bool PAIR_ = false,
-          int MAX_EXPERTS_ = 1024>
+          int MAX_EXPERTS_ = 1024, int KS_ = 1>
 struct GemmCfg {
   static constexpr int BN = BN_;          // MMA N: rows of operand B per tile
   static constexpr int STAGES = STAGES_;  // shared-memory pipeline depth
@@ -95,13 +95,20 @@ struct GemmCfg {
   static constexpr bool PAIR = PAIR_;
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int BM = 128;          // MMA M: rows of operand A per tile (per CTA)
-  static constexpr int KSTAGE = 256;      // K elements per stage = one 128-byte TMA row
+  // KS: 256-wide K steps per ring stage.  KS = 2 (CTA pairs) lands two K steps of each operand
+  // with one 3-D copy (box of 2 x 128-byte rows): the copy engine's cost per instruction, not
+  // its bytes, bounded the pair's stage rate, and this halves the instructions per MMA.
+  static constexpr int KS = KS_;
+  static constexpr int KSTAGE = 256 * KS;  // K elements per stage
+  static constexpr int MMAS = KSTAGE / 64;  // MMAs (K = 64) per full stage
+  static constexpr int A_TILE = BM * 128;  // bytes of one 256-wide K step of A (one swizzled tile)
   static constexpr int VEC = MX ? 32 : 16;
   static constexpr int CHUNKS = KSTAGE / VEC / 4;  // 512-byte scale chunks per 128 rows per stage
   static constexpr int SFB_BLOCKS = (BN + 127) / 128;
-  static constexpr int A_BYTES = BM * 128;
+  static constexpr int A_BYTES = BM * 128 * KS;
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of operand B a CTA stages
-  static constexpr int B_BYTES = B_ROWS * 128;
+  static constexpr int B_TILE = B_ROWS * 128;
+  static constexpr int B_BYTES = B_TILE * KS;
   static constexpr int SFA_BYTES = CHUNKS * 512;
   static constexpr int SFB_BYTES = SFB_BLOCKS * CHUNKS * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
@@ -124,7 +131,7 @@ struct GemmCfg {
   // A pair adds warp 10, which copies the scales into a ring of their own (SF_STAGES deep) ahead
   // of the operands, so that writing them to tensor memory is off the operand ring's critical
   // path and the producer issues two copies per stage instead of five.
-  static constexpr int SF_STAGES = PAIR ? 5 : STAGES;
+  static constexpr int SF_STAGES = PAIR ? (KS == 2 ? 2 : 5) : STAGES;
   static constexpr int THREADS = PAIR ? 352 : 320;
   // The ring keeps each operand in a region of its own (stage i of A at A_REGION + i * A_BYTES,
   // and so on), so the stages of one operand are contiguous and a CTA whose whole K slice fits
@@ -160,6 +167,7 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
   static_assert(!PAIR || (MULTI_TILE && BN == 256 && !MX), "CTA pairs: NVFP4 256-wide whole tiles only");
+  static_assert(KS == 1 || (KS == 2 && PAIR), "two K steps per stage: CTA pairs only");
 };
 
 struct GemmArgs {
@@ -362,13 +370,22 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs &p, const Tables<C,
   return t;
 }
 
-// Chunks / MMAs in K stage kt: the last stage may be short (K % 256 != 0).
+// Chunks / MMAs in K stage kt: the last stage may be short (K % KSTAGE != 0).
 template <class C>
 __device__ __forceinline__ int stage_chunks(const GemmArgs &p, int kt) {
   return min(C::CHUNKS, p.sf_chunks - kt * C::CHUNKS);
 }
+template <class C = GemmCfg<32, 4, false>>
 __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
-  return min(4, (p.k - kt * 256 + 63) / 64);
+  return min(C::MMAS, (p.k - kt * C::KSTAGE + 63) / 64);
+}
+
+// Operand tile of K stage kt: KS = 1 a 2-D box at byte column kt * 128; KS = 2 a 3-D box of two
+// 256-wide K steps from the stage view (z = K step), landing as two consecutive tiles.
+template <class C>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, uint32_t bar, int kt, int row) {
+  if constexpr (C::KS == 1) tma_load_2d(dst, map, bar, kt * 128, row);
+  else tma_load_3d(dst, map, bar, 0, row, kt * C::KS);
 }
 
 // Copies of K stage kt into ring slot stg (only the requested operand halves), all issued by the
@@ -381,13 +398,13 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
   const int nch = stage_chunks<C>(p, kt);
   const uint32_t bar = smem_u32(&full[stg]);
   if (do_a) {
-    tma_load_2d(smem_u32(smem + stg * C::A_BYTES), tmA, bar, kt * 128, t.a_y);
+    load_operand<C>(smem_u32(smem + stg * C::A_BYTES), tmA, bar, kt, t.a_y);
     if constexpr (!C::PAIR)  // (a pair's scales go through their own ring)
       bulk_load(smem_u32(smem + C::SFA_REGION + stg * C::SFA_BYTES),
                 t.sfa_blk + static_cast<int64_t>(kt) * C::CHUNKS * 512, nch * 512, bar);
   }
   if (do_b && !FUSED) {
-    tma_load_2d(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt * 128, t.b_y);
+    load_operand<C>(smem_u32(smem + C::B_REGION + stg * C::B_BYTES), tmB, bar, kt, t.b_y);
     if constexpr (!C::PAIR)
       for (int b = 0; b < t.sfb_blocks; ++b)
         bulk_load(smem_u32(smem + C::SFB_REGION + stg * C::SFB_BYTES + b * C::CHUNKS * 512),
@@ -922,14 +939,19 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           } else {
             const uint32_t sb = slot + C::SFA_COLS;
             constexpr uint32_t SB = 4 * C::SFB_BLOCKS;  // B scale columns per MMA
-            if (stage_mmas(p, kt) == 4) {
-              mma_nvf4<C::CG>(d_tmem, adesc, bdesc, C::IDESC, slot, sb, acc0);
-              mma_nvf4<C::CG>(d_tmem, adesc + 2, bdesc + 2, C::IDESC, slot + 4, sb + SB, 1u);
-              mma_nvf4<C::CG>(d_tmem, adesc + 4, bdesc + 4, C::IDESC, slot + 8, sb + 2 * SB, 1u);
-              mma_nvf4<C::CG>(d_tmem, adesc + 6, bdesc + 6, C::IDESC, slot + 12, sb + 3 * SB, 1u);
+            // K step j of the stage: 32 bytes into its 256-wide tile (descriptor units of 16
+            // bytes), tile j / 4 of a KS = 2 stage at +A_TILE / +B_TILE
+            const int nm = stage_mmas<C>(p, kt);
+            if (nm == C::MMAS) {
+#pragma unroll
+              for (int j = 0; j < C::MMAS; ++j)
+                mma_nvf4<C::CG>(d_tmem, adesc + 2 * (j & 3) + (j >> 2) * (C::A_TILE >> 4),
+                                bdesc + 2 * (j & 3) + (j >> 2) * (C::B_TILE >> 4), C::IDESC, slot + 4 * j, sb + j * SB,
+                                j > 0 ? 1u : acc0);
             } else {
-              for (int j = 0; j < stage_mmas(p, kt); ++j)
-                mma_nvf4<C::CG>(d_tmem, adesc + 2 * j, bdesc + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB,
+              for (int j = 0; j < nm; ++j)
+                mma_nvf4<C::CG>(d_tmem, adesc + 2 * (j & 3) + (j >> 2) * (C::A_TILE >> 4),
+                                bdesc + 2 * (j & 3) + (j >> 2) * (C::B_TILE >> 4), C::IDESC, slot + 4 * j, sb + j * SB,
                                 j > 0 ? 1u : acc0);
             }
           }

@@ -260,6 +260,11 @@ __device__ __forceinline__ void tmem_st_32x32b<32>(uint32_t taddr, const uint32_
       "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+template <>
+__device__ __forceinline__ void tmem_st_32x32b<64>(uint32_t taddr, const uint32_t *v) {
+  tmem_st_32x32b<32>(taddr, v);
+  tmem_st_32x32b<32>(taddr + 32, v + 32);
+}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }

@@ -68,7 +68,10 @@ def test_stream_k_splits(nv, m, n, k):
 @pytest.mark.parametrize("m,n,k", [
     (300, 13056, 512),    # 2 row tiles: the second CTA of each last-row pair is past M (stores nothing)
     (520, 9984, 544),     # 8 valid rows in the last pair tile, K tail of 32 (a short last stage)
-    (2304, 4096, 1024)])  # 144 tiles over 76 pairs: accumulators handed back across CTAs
+    (2304, 4096, 1024),   # 144 tiles over 76 pairs: accumulators handed back across CTAs
+    (264, 14336, 1280),   # 2 K steps per stage, the last stage holding one (its second is zero-filled)
+    (160, 12288, 768),    # fewer than 256 rows on pairs (M > 128 with many tiles), a half last stage
+    (1024, 4096, 2560)])  # 64 tiles: one per pair, 5 two-step stages
 def test_cta_pair_tiles(nv, m, n, k):
     """256 x 256 tiles computed by CTA pairs (cta_group::2): every output element checked."""
     p = nv.nvfp4_gemm_plan(m, n, k)
@@ -119,10 +122,21 @@ def test_decode_sweep_full_size(nv, m):
     assert_within(d, R, tol, f"decode M={m}")
 
 
+def test_prefill_4096_every_element(nv):
+    """4096 x 4096 x 7168 (CTA pairs, 256 tiles over 76 pairs, 14 two-step stages per tile), every
+    output element against the fp64 oracle."""
+    m, n, k = 4096, 4096, 7168
+    assert nv.nvfp4_gemm_plan(m, n, k)["tile_m"] == 256
+    ops = nvfp4_operands(m, n, k, 0)
+    d = _run(nv, ops)
+    R, tol = reference(ops)
+    assert_within(d, R, tol, f"prefill {m}x{n}x{k}, all elements")
+
+
 @pytest.mark.parametrize("m,n,k", [(1024, 4096, 7168), (2048, 4096, 7168), (4096, 4096, 7168), (4096, 4096, 4096),
                                    (128, 7168, 2048)])
 def test_prefill_sampled_rows(nv, m, n, k):
-    """The five prefill shapes at full size (M = 2048 and 4096 run on CTA pairs), checked on whole
+    """The five prefill shapes at full size (M >= 1024 run on CTA pairs), checked on whole
     128-row blocks at both ends plus seeded rows."""
     ops = nvfp4_operands(m, n, k, 0)
     d = _run(nv, ops)
