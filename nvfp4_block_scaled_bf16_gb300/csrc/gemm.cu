@@ -129,7 +129,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
     case 32: pl.stages = 4; break;
     case 64: pl.stages = 7; break;
     case 128: pl.stages = 6; break;
-    default: pl.stages = pl.pair ? (pl.ks == 2 ? 3 : 6) : 4; break;
+    default: pl.stages = pl.pair ? (pl.ks == 2 ? 3 : 5) : 4; break;
   }
   // A swap-AB CTA holds one tile; when its whole K slice fits the ring (and K is a whole number of
   // 256-wide stages), the activation and both scale slices land with one copy each.
@@ -162,7 +162,7 @@ nvfp4_status_t with_config(const Plan &pl, F &&f) {
     case 128: return pl.swap ? f(GemmCfg<128, 6, false, false>{}) : f(GemmCfg<128, 6, false, true>{});
     default:
       if (pl.swap) return f(GemmCfg<256, 4, false, false>{});
-      return pl.ks == 2 ? f(GemmCfg<256, 3, false, true, 1, true, 1024, 2>{}) : f(GemmCfg<256, 6, false, true, 1, true>{});
+      return pl.ks == 2 ? f(GemmCfg<256, 3, false, true, 1, true, 1024, 2>{}) : f(GemmCfg<256, 5, false, true, 1, true>{});
   }
 }
 

@@ -16,32 +16,38 @@
 //               lands B and both scale slices with one copy each and A stage by stage, the
 //               first copies going out before the rest of the CTA is set up; weight-streaming
 //               CTAs keep at most `lookahead` stages in flight so cold HBM returns them in order;
-//   warp 1      allocates tensor memory; one lane issues 4 MMAs (K = 64 each) per 256-wide K
-//               stage, then commits the stage back to the producer and the scale slot back to
-//               the scale writers, and after the last K stage of a tile the accumulator to the
-//               epilogue;
+//   warp 1      allocates tensor memory; one lane issues the MMAs (K = 64 each; 4 per 256-wide
+//               K step), waiting once per K step for its scale slot, commits each scale slot
+//               back to the scale writers and each stage back to the producer, and after the
+//               last stage of a tile the accumulator to the epilogue;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quadrant, alpha * acc in fp32, one RNE
-//               conversion to bf16, 256-bit stores (in the fused-quantisation kernels they
-//               first quantise the bf16 activation into the operand-B stages);
-//   warps 6..9  scale writers: each reads the stage's scale tiles from shared memory and
-//               writes them into its own quadrant of a tensor-memory scale slot with
-//               tcgen05.st (SF_SLOTS slots in a ring; a resident CTA fills one slot per stage
-//               with a single hand-off to the MMA lane), keeping those writes off the tensor pipe
-//               (a tcgen05.cp of one 512-byte tile occupies the pipe about as long as 40 % of a
-//               128x256x64 MMA);
+//               conversion to bf16; dense CTAs that walk whole tiles stage each 32-column chunk
+//               in shared memory and write it with one tensor store, the others store 256-bit
+//               vectors per row (in the fused-quantisation kernels they first quantise the
+//               bf16 activation into the operand-B stages);
+//   warps 6..9  scale writers: each waits until the stage's operands (and scales) have landed,
+//               reads the scale tiles from shared memory and writes them into its own quadrant
+//               of a tensor-memory scale slot with tcgen05.st (one slot per 256-wide K step,
+//               SF_SLOTS in a ring; a resident CTA fills one slot per stage with a single
+//               hand-off to the MMA lane).  Their arrival is the MMA lane's only wait per K step.
+//               Copying the scales with tcgen05.cp from the MMA lane instead was measured to
+//               cap a 128x256x256 step at ~840 cycles against 520 of MMA: the copy unit takes
+//               ~55 cycles per 512-byte tile and such a step needs 12 of them;
 //   warp 10     (pairs only) copies the scales into a ring of their own, ahead of the operands.
 // NACC accumulator buffers let the epilogue of tile t overlap the mainloop of tile t+1.
 //
 // CTA pairs (PAIR, 256 x 256 tiles for large M): a cluster of two CTAs runs cta_group::2 MMAs
 // (M = 256, issued by the first CTA; a 256x256x64 MMA occupies the pipe for the same ~128 cycles
 // as a 128x256x64 one on a single CTA).  Each CTA stages its 128 rows of A and its 128 rows of B;
-// the scales of its A rows and of all 256 B rows go through a separate 5-slot ring that warp 10
-// fills ahead of the operands, so the producer issues two copies per stage.  The hand-offs
-// across the pair: the second CTA's MMA warp (which issues no MMAs) relays "stage landed", its
-// scale writers and epilogue arrive on the first CTA's barriers, and the first CTA's commits
-// arrive on both CTAs' barriers (multicast).  Arrivals use the default CTA-scope release: a
-// cluster-scope release measured 1000-1500 cycles per arrive; every arrival follows the
-// completion of what it announces (tcgen05.wait::st / ::ld, a completed barrier).
+// the scales of its A rows and of all 256 B rows go through a separate ring that warp 10 fills
+// ahead of the operands.  When K allows, a stage holds two 256-wide K steps, landed with one 3-D
+// copy per operand (the copy engine's cost per instruction bounded the one-step stage).  The
+// hand-offs across the pair: the second CTA's scale writers and epilogue arrive on the first
+// CTA's barriers (the writers only after their own CTA's operands landed, so the first CTA's
+// MMA lane needs no other signal from its peer), and the first CTA's commits arrive on both
+// CTAs' barriers (multicast).  Arrivals use the default CTA-scope release: a cluster-scope
+// release measured 1000-1500 cycles per arrive; every arrival follows the completion of what it
+// announces (tcgen05.wait::st / ::ld, a completed barrier).
 //
 // Work decomposition: each CTA walks a list of segments (tile, K-stage range).
 //   - whole tiles: CTA c takes tiles c, c+G, c+2G, ... below dp_tiles (G = grid size; for
@@ -112,8 +118,12 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = CHUNKS * 512;
   static constexpr int SFB_BYTES = SFB_BLOCKS * CHUNKS * 512;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-  static constexpr int SFA_COLS = CHUNKS * 4;
-  static constexpr int SFB_COLS = SFB_BLOCKS * CHUNKS * 4;
+  // Tensor-memory scale slots hold one 256-wide K step each (SUB slots per ring stage), so that
+  // the scale writers can run ahead of the MMAs by several K steps even when a stage holds two.
+  static constexpr int SUB = KS;                     // scale slots per ring stage
+  static constexpr int SUB_CHUNKS = CHUNKS / SUB;    // 512-byte chunks per 128 rows per slot
+  static constexpr int SFA_COLS = SUB_CHUNKS * 4;
+  static constexpr int SFB_COLS = SFB_BLOCKS * SUB_CHUNKS * 4;
   static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // columns of one scale slot
   // a second accumulator only helps CTAs that walk several tiles (epilogue of tile t overlaps
   // the mainloop of t+1)
@@ -122,6 +132,9 @@ struct GemmCfg {
   // Tensor-memory scale slots: one per ring stage for single-tile (swap-AB) CTAs, so a CTA
   // whose K slice fits the ring writes every stage's scales once, with no slot reuse.
   static constexpr int SF_SLOTS = !MULTI_TILE_ ? STAGES : (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
+  // The slots of one stage form a group with one written / free barrier pair, so that the MMA
+  // lane waits and commits once per stage whatever the number of K steps in it.
+  static constexpr int SF_GROUPS = SF_SLOTS / SUB;
   static constexpr int TMEM_USED = SF_COL0 + SF_SLOTS * SF_SLOT;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int RED_BYTES = BM * BN * 4;  // partial tile: cluster split-K buffer, stream-K slot
@@ -157,7 +170,7 @@ struct GemmCfg {
   // arrive on the first CTA's)
   static constexpr int SLOT_ARRIVALS = PAIR ? 8 : 4;
   static constexpr int ACC_ARRIVALS = PAIR ? 8 : 4;
-  static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8, "tensor memory budget, scale-slot barriers");
+  static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8 && SF_SLOTS % SUB == 0, "tensor memory budget, scale-slot barriers");
   static_assert(STAGES <= 7 && SF_STAGES <= 8 && (2 * STAGES + 46) * 8 + 8 * 4 <= CTRL_BYTES,
                 "barriers and flags fit the control block");
   static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
@@ -382,10 +395,17 @@ __device__ __forceinline__ int stage_mmas(const GemmArgs &p, int kt) {
 
 // Operand tile of K stage kt: KS = 1 a 2-D box at byte column kt * 128; KS = 2 a 3-D box of two
 // 256-wide K steps from the stage view (z = K step), landing as two consecutive tiles.
+// A CTA pair's copies complete on the first CTA's barrier (`bar` is then a shared::cluster
+// address), so that one barrier there tells the MMA lane that both CTAs' operands have landed.
 template <class C>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap *map, uint32_t bar, int kt, int row) {
-  if constexpr (C::KS == 1) tma_load_2d(dst, map, bar, kt * 128, row);
-  else tma_load_3d(dst, map, bar, 0, row, kt * C::KS);
+  if constexpr (C::PAIR) {
+    if constexpr (C::KS == 1) tma_load_2d_pair(dst, map, bar, kt * 128, row);
+    else tma_load_3d_pair(dst, map, bar, 0, row, kt * C::KS);
+  } else {
+    if constexpr (C::KS == 1) tma_load_2d(dst, map, bar, kt * 128, row);
+    else tma_load_3d(dst, map, bar, 0, row, kt * C::KS);
+  }
 }
 
 // Copies of K stage kt into ring slot stg (only the requested operand halves), all issued by the
@@ -396,7 +416,7 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
                                             uint64_t *full, const CUtensorMap *tmA, const CUtensorMap *tmB,
                                             bool do_a, bool do_b) {
   const int nch = stage_chunks<C>(p, kt);
-  const uint32_t bar = smem_u32(&full[stg]);
+  const uint32_t bar = C::PAIR ? map_to_rank(smem_u32(&full[stg]), 0) : smem_u32(&full[stg]);
   if (do_a) {
     load_operand<C>(smem_u32(smem + stg * C::A_BYTES), tmA, bar, kt, t.a_y);
     if constexpr (!C::PAIR)  // (a pair's scales go through their own ring)
@@ -415,7 +435,7 @@ __device__ __forceinline__ void issue_stage(const GemmArgs &p, const TileInfo &t
 // Bytes that land on full[] for K stage kt (operands, and scales unless they have their own ring).
 template <class C, bool FUSED = false>
 __device__ __forceinline__ uint32_t stage_tx(const GemmArgs &p, const TileInfo &t, int kt) {
-  if constexpr (C::PAIR) return C::A_BYTES + C::B_BYTES;
+  if constexpr (C::PAIR) return 2 * (C::A_BYTES + C::B_BYTES);  // both CTAs' operands, on the first CTA's barrier
   else if constexpr (FUSED) return C::A_BYTES + stage_chunks<C>(p, kt) * 512;  // B is quantised in-kernel
   else return C::A_BYTES + C::B_BYTES + stage_chunks<C>(p, kt) * 512 * (1 + t.sfb_blocks);
 }
@@ -618,12 +638,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
   uint64_t *accf = empty + C::STAGES;
   uint64_t *acce = accf + 2;
   uint64_t *sff = acce + 2;           // scale slot written (the scale writers arrive: 4, 8 in a pair)
-  uint64_t *sfe = sff + 8;            // scale slot free (MMA commit)
-  uint64_t *drain = sfe + 8;
+  uint64_t *drain = sff + 16;
   uint64_t *sf_full = drain + 1;       // pair: scale ring slot landed
   uint64_t *sf_empty = sf_full + 8;    // pair: scale ring slot read by the 4 scale writers
-  uint64_t *peer_full = sf_empty + 8;  // pair (first CTA): the second CTA's operand stage landed
-  uint64_t *rbar = peer_full + 8;      // push reduction: this rank's slices received
+  uint64_t *rbar = sf_empty + 16;     // push reduction: this rank's slices received
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(rbar + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
   volatile int *consumed = abort_flag + 1;  // K stages the MMA lane has taken (abort drain)
@@ -655,9 +673,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       mbar_init(smem_u32(&accf[a]), 1);
       mbar_init(smem_u32(&acce[a]), C::ACC_ARRIVALS);
     }
-    for (int q = 0; q < C::SF_SLOTS; ++q) {
+    for (int q = 0; q < C::SF_GROUPS; ++q) {
       mbar_init(smem_u32(&sff[q]), C::SLOT_ARRIVALS);
-      mbar_init(smem_u32(&sfe[q]), 1);
     }
     mbar_init(smem_u32(drain), 1);
     mbar_init(smem_u32(rbar), 1);
@@ -666,7 +683,6 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         mbar_init(smem_u32(&sf_full[j]), 1);
         mbar_init(smem_u32(&sf_empty[j]), 4);
       }
-      for (int s = 0; s < C::STAGES; ++s) mbar_init(smem_u32(&peer_full[s]), 1);
     }
     *sf_issued = 0;
     *abort_flag = 0;
@@ -797,7 +813,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
           pre = min(p.lookahead > 0 ? p.lookahead : C::STAGES, min(C::STAGES, s0.kt1 - s0.kt0));
           for (int i = 0; i < pre; ++i) {  // the ring is empty at start: no wait for a free slot
             const int kt = s0.kt0 + i;
-            mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx<C, FUSED>(p, t, kt));
+            if (crank == 0) mbar_arrive_expect_tx(smem_u32(&full[i]), stage_tx<C, FUSED>(p, t, kt));
             if (!(skip_first && i == 0)) issue_stage<C, FUSED>(p, t, kt, i, smem, full, &tmA, &tmB, pre_a, pre_b);
           }
           if (C::SWAP_ONLY && pre_a) {
@@ -821,7 +837,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
             }
             if (!early_stage) {
               if (!mbar_wait<C::PAIR>(smem_u32(&empty[stage]), phase ^ 1, wc, kSiteLoadEmpty)) goto producer_done;
-              mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx<C, FUSED>(p, t, kt));
+              if (crank == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), stage_tx<C, FUSED>(p, t, kt));
             }
             const bool do_a = !(early_stage && pre_a), do_b = !(early_stage && pre_b);
             if (!(skip_first && issued == 0) && (do_a || do_b))
@@ -876,90 +892,87 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       }
     mma_done_r:
       *consumed = taken;
-    } else if (C::PAIR && lane == 0 && crank == 1) {
-      // Relay of the pair's second CTA (which issues no MMAs): tells the first CTA's MMA lane
-      // when each operand stage of this CTA has landed.
-      int stage = 0;
-      uint32_t phase = 0;
-      Work w = work0;
-      for (Seg sg; w.next(p, sg);) {
-        for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteMmaFull)) goto relay_done;
-          mbar_arrive_remote(map_to_rank(smem_u32(&peer_full[stage]), 0));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-    relay_done:;
     } else if (lane == 0 && crank == 0) {
       int stage = 0;
-      uint32_t phase = 0;  // of full[] / peer_full[] (pairs wait on them; others rely on sff)
+      uint32_t phase = 0;  // of full[] (pairs wait on it; for the others sff implies it)
       int taken = 0;  // stages known landed (abort drain)
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t it = 0;
+      int g = 0;             // scale-slot group of the stage
+      uint32_t g_phase = 0;
+      // Per stage the lane waits once for the scale group (and, in a pair, once for the operands),
+      // issues the stage's MMAs and commits twice; the descriptors of stage 0 are computed once
+      // (the other stages sit at fixed offsets), so that the lane's own work between MMAs stays
+      // below the tensor pipe's time for them.
+      const uint64_t adesc0 = sdesc_k_sw128(smem_u32(smem));
+      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(smem + C::B_REGION));
+      const uint32_t sf_base = tmem + C::SF_COL0;
       Work w = work0;
       for (Seg sg; w.next(p, sg);) {
         if (!mbar_wait<C::PAIR>(smem_u32(&acce[acc]), acc_phase ^ 1, wc, kSiteMmaAcc)) goto mma_done;
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * C::BN;
-        for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
-          const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-          if (!mbar_wait<C::PAIR>(smem_u32(&sff[s_idx]), s_round & 1, wc, kSiteMmaScale)) goto mma_done;
+        for (int kt = sg.kt0; kt < sg.kt1; ++kt) {
+          if (!mbar_wait(smem_u32(&sff[g]), g_phase, wc, kSiteMmaScale)) goto mma_done;
           if constexpr (C::PAIR) {
-            // a pair's scale writers do not wait for the operands: the stage's A and B halves
-            // of both CTAs are waited for here
+            // a pair's scale writers do not wait for the operands: both CTAs' operand copies of
+            // the stage complete on this CTA's barrier
             if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteMmaFull)) goto mma_done;
-            if (!mbar_wait<true>(smem_u32(&peer_full[stage]), phase, wc, kSiteMmaFull)) goto mma_done;
           }
           ++taken;
           tc_fence_after();
-          const uint32_t slot = tmem + C::SF_COL0 + s_idx * C::SF_SLOT;
-          const uint64_t adesc = sdesc_k_sw128(smem_u32(smem + stage * C::A_BYTES));
-          const uint64_t bdesc = sdesc_k_sw128(smem_u32(smem + C::B_REGION + stage * C::B_BYTES));
+          const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (C::A_BYTES >> 4));
+          const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (C::B_BYTES >> 4));
           const uint32_t acc0 = kt > sg.kt0 ? 1u : 0u;
-          if constexpr (C::MX) {
-            // MXFP4: a 512-byte scale chunk covers 128 K elements = two MMAs (scale ids 0, 2)
-            constexpr uint32_t I0 = C::IDESC, I2 = C::IDESC | (2u << 29) | (2u << 4);
-            const uint32_t sb = slot + C::SFA_COLS;
-            if (stage_mmas(p, kt) == 4) {
-              mma_mxf4(d_tmem, adesc, bdesc, I0, slot, sb, acc0);
-              mma_mxf4(d_tmem, adesc + 2, bdesc + 2, I2, slot, sb, 1u);
-              mma_mxf4(d_tmem, adesc + 4, bdesc + 4, I0, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
-              mma_mxf4(d_tmem, adesc + 6, bdesc + 6, I2, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
+          // K step h of the stage reads its scales from slot g * SUB + h
+#pragma unroll
+          for (int h = 0; h < C::SUB; ++h) {
+            const uint32_t slot = sf_base + (g * C::SUB + h) * C::SF_SLOT;
+            if constexpr (C::MX) {
+              // MXFP4: a 512-byte scale chunk covers 128 K elements = two MMAs (scale ids 0, 2)
+              constexpr uint32_t I0 = C::IDESC, I2 = C::IDESC | (2u << 29) | (2u << 4);
+              const uint32_t sb = slot + C::SFA_COLS;
+              if (stage_mmas(p, kt) == 4) {
+                mma_mxf4(d_tmem, adesc, bdesc, I0, slot, sb, acc0);
+                mma_mxf4(d_tmem, adesc + 2, bdesc + 2, I2, slot, sb, 1u);
+                mma_mxf4(d_tmem, adesc + 4, bdesc + 4, I0, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
+                mma_mxf4(d_tmem, adesc + 6, bdesc + 6, I2, slot + 4, sb + 4 * C::SFB_BLOCKS, 1u);
+              } else {
+                for (int j = 0; j < stage_mmas(p, kt); ++j) {
+                  const int c = j >> 1;
+                  mma_mxf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, (j & 1) ? I2 : I0, slot + 4 * c,
+                           sb + c * 4 * C::SFB_BLOCKS, j > 0 ? 1u : acc0);
+                }
+              }
             } else {
-              for (int j = 0; j < stage_mmas(p, kt); ++j) {
-                const int c = j >> 1;
-                mma_mxf4(d_tmem, adesc + 2 * j, bdesc + 2 * j, (j & 1) ? I2 : I0, slot + 4 * c,
-                         sb + c * 4 * C::SFB_BLOCKS, j > 0 ? 1u : acc0);
+              const uint32_t sb = slot + C::SFA_COLS;
+              constexpr uint32_t SB = 4 * C::SFB_BLOCKS;  // B scale columns per MMA
+              // MMA j of K step h: 32 bytes into the step's 128-byte-row tile (descriptor units of
+              // 16 bytes), the step's tile at +h * A_TILE / +h * B_TILE
+              const uint64_t ad = adesc + h * (C::A_TILE >> 4), bd = bdesc + h * (C::B_TILE >> 4);
+              const int nm = stage_mmas<C>(p, kt) - 4 * h;
+              if (nm >= 4) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  mma_nvf4<C::CG>(d_tmem, ad + 2 * j, bd + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB,
+                                  (j > 0 || h > 0) ? 1u : acc0);
+              } else {
+                for (int j = 0; j < nm; ++j)
+                  mma_nvf4<C::CG>(d_tmem, ad + 2 * j, bd + 2 * j, C::IDESC, slot + 4 * j, sb + j * SB,
+                                  (j > 0 || h > 0) ? 1u : acc0);
               }
             }
-          } else {
-            const uint32_t sb = slot + C::SFA_COLS;
-            constexpr uint32_t SB = 4 * C::SFB_BLOCKS;  // B scale columns per MMA
-            // K step j of the stage: 32 bytes into its 256-wide tile (descriptor units of 16
-            // bytes), tile j / 4 of a KS = 2 stage at +A_TILE / +B_TILE
-            const int nm = stage_mmas<C>(p, kt);
-            if (nm == C::MMAS) {
-#pragma unroll
-              for (int j = 0; j < C::MMAS; ++j)
-                mma_nvf4<C::CG>(d_tmem, adesc + 2 * (j & 3) + (j >> 2) * (C::A_TILE >> 4),
-                                bdesc + 2 * (j & 3) + (j >> 2) * (C::B_TILE >> 4), C::IDESC, slot + 4 * j, sb + j * SB,
-                                j > 0 ? 1u : acc0);
-            } else {
-              for (int j = 0; j < nm; ++j)
-                mma_nvf4<C::CG>(d_tmem, adesc + 2 * (j & 3) + (j >> 2) * (C::A_TILE >> 4),
-                                bdesc + 2 * (j & 3) + (j >> 2) * (C::B_TILE >> 4), C::IDESC, slot + 4 * j, sb + j * SB,
-                                j > 0 ? 1u : acc0);
-            }
           }
+          // (one commit: the scale writers learn from the same barrier that the stage's scale
+          // group is free again)
           commit_to<C>(smem_u32(&empty[stage]));
-          commit_to<C>(smem_u32(&sfe[s_idx]));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
+          }
+          if (++g == C::SF_GROUPS) {
+            g = 0;
+            g_phase ^= 1;
           }
         }
         commit_to<C>(smem_u32(&accf[acc]));
@@ -979,7 +992,8 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t it = 0;
+    int g = 0;  // scale-slot group of the stage
+    uint32_t g_phase = 0;
     Work w = work0;
     if (!GROUPED && p.resident) {
       // Resident slice: all scale slices landed with stage 0; fill every stage's slot, then
@@ -1017,55 +1031,72 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sff[0]));
       }
-    } else
-    for (Seg sg; w.next(p, sg);) {
-      for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++it) {
-        const uint32_t s_idx = it % C::SF_SLOTS, s_round = it / C::SF_SLOTS;
-        if (!mbar_wait<C::PAIR>(smem_u32(&sfe[s_idx]), (s_round & 1) ^ 1, wc, kSiteScaleSlot)) goto scale_done;
-        // The stage's scales land with its operands, or (pair) in the scale ring ahead of them.
-        const int sf_slot = C::PAIR ? static_cast<int>(it % C::SF_STAGES) : stage;
-        if constexpr (C::PAIR) {
-          if (!mbar_wait(smem_u32(&sf_full[sf_slot]), (it / C::SF_STAGES) & 1, wc, kSiteScaleFull)) goto scale_done;
-        } else {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
-        }
-        const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + sf_slot * C::SFA_BYTES);
-        const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + sf_slot * C::SFB_BYTES);
-        uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
-#pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c) {
-          const uint4 v = ld_sf_lane(sfa_s + 512 * c, lane, p.sf_sm103);
-          ra[4 * c] = v.x;
-          ra[4 * c + 1] = v.y;
-          ra[4 * c + 2] = v.z;
-          ra[4 * c + 3] = v.w;
-#pragma unroll
-          for (int b = 0; b < C::SFB_BLOCKS; ++b) {
-            const uint4 w = ld_sf_lane(sfb_s + (b * C::CHUNKS + c) * 512, lane, p.sf_sm103);
-            const int o = c * 4 * C::SFB_BLOCKS + 4 * b;
-            rb[o] = w.x;
-            rb[o + 1] = w.y;
-            rb[o + 2] = w.z;
-            rb[o + 3] = w.w;
+    } else {
+      uint32_t sit = 0;  // ring stages (the scale ring of a pair is indexed by stage)
+      for (Seg sg; w.next(p, sg);) {
+        for (int kt = sg.kt0; kt < sg.kt1; ++kt, ++sit) {
+          // The stage's scales land with its operands, or (pair) in the scale ring ahead of them.
+          const int sf_slot = C::PAIR ? static_cast<int>(sit % C::SF_STAGES) : stage;
+          if constexpr (C::PAIR) {
+            if (!mbar_wait(smem_u32(&sf_full[sf_slot]), (sit / C::SF_STAGES) & 1, wc, kSiteScaleFull)) goto scale_done;
+          } else {
+            if (!mbar_wait(smem_u32(&full[stage]), phase, wc, kSiteScaleFull)) goto scale_done;
           }
-        }
-        const uint32_t slot = tmem + lane_base + C::SF_COL0 + s_idx * C::SF_SLOT;
-        tmem_st_32x32b<C::SFA_COLS>(slot, ra);
-        tmem_st_32x32b<C::SFB_COLS>(slot + C::SFA_COLS, rb);
-        if constexpr (C::PAIR) {  // the scales are in registers: the ring slot may be refilled
+          const uint32_t sfa_s = smem_u32(smem + C::SFA_REGION + sf_slot * C::SFA_BYTES);
+          const uint32_t sfb_s = smem_u32(smem + C::SFB_REGION + sf_slot * C::SFB_BYTES);
+          // The stage's group of tensor-memory slots, one per 256-wide K step (chunks h * SUB_CHUNKS ..),
+          // was last read by the MMAs of stage sit - SF_GROUPS; their completion is the phase
+          // (sit - SF_GROUPS) / STAGES of that stage's ring barrier empty[], which the MMA lane
+          // commits to (both CTAs' of a pair).  The writers are never a full ring turn behind
+          // the MMAs (those need this stage's scales first), so the parity is unambiguous.
+          if (sit >= static_cast<uint32_t>(C::SF_GROUPS)) {
+            const uint32_t done = sit - C::SF_GROUPS;
+            if (!mbar_wait(smem_u32(&empty[done % C::STAGES]), (done / C::STAGES) & 1, wc, kSiteScaleSlot)) goto scale_done;
+          }
+#pragma unroll
+          for (int h = 0; h < C::SUB; ++h) {
+            uint32_t ra[C::SFA_COLS], rb[C::SFB_COLS];
+#pragma unroll
+            for (int cc = 0; cc < C::SUB_CHUNKS; ++cc) {
+              const int c = h * C::SUB_CHUNKS + cc;
+              const uint4 v = ld_sf_lane(sfa_s + 512 * c, lane, p.sf_sm103);
+              ra[4 * cc] = v.x;
+              ra[4 * cc + 1] = v.y;
+              ra[4 * cc + 2] = v.z;
+              ra[4 * cc + 3] = v.w;
+#pragma unroll
+              for (int b = 0; b < C::SFB_BLOCKS; ++b) {
+                const uint4 w = ld_sf_lane(sfb_s + (b * C::CHUNKS + c) * 512, lane, p.sf_sm103);
+                const int o = cc * 4 * C::SFB_BLOCKS + 4 * b;
+                rb[o] = w.x;
+                rb[o + 1] = w.y;
+                rb[o + 2] = w.z;
+                rb[o + 3] = w.w;
+              }
+            }
+            const uint32_t slot = tmem + lane_base + C::SF_COL0 + (g * C::SUB + h) * C::SF_SLOT;
+            tmem_st_32x32b<C::SFA_COLS>(slot, ra);
+            tmem_st_32x32b<C::SFB_COLS>(slot + C::SFA_COLS, rb);
+          }
+          if constexpr (C::PAIR) {  // the stage's scales are in registers: the ring slot may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sf_empty[sf_slot]));
+          }
+          tmem_st_wait();
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&sf_empty[sf_slot]));
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if constexpr (C::PAIR) mbar_arrive_remote(map_to_rank(smem_u32(&sff[s_idx]), 0));
-          else mbar_arrive(smem_u32(&sff[s_idx]));
-        }
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
+          if (lane == 0) {
+            if constexpr (C::PAIR) mbar_arrive_remote(map_to_rank(smem_u32(&sff[g]), 0));
+            else mbar_arrive(smem_u32(&sff[g]));
+          }
+          if (++g == C::SF_GROUPS) {
+            g = 0;
+            g_phase ^= 1;
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
       }
     }
@@ -1243,7 +1274,9 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
     // Drain: wait (bounded) for copies still landing in shared memory and for outstanding
     // tcgen05 operations, so nothing writes shared or tensor memory after the CTA is gone.
     if (threadIdx.x == 0) {
-      const int issued = *issued_count;
+      // (a pair's operand copies complete on the first CTA's barriers: the first CTA drains them
+      // for both, and the second stays until then at the cluster barrier before exit)
+      const int issued = crank == 0 ? *issued_count : 0;
       const int done = *consumed;
       for (int i = (done > issued - C::STAGES ? done : issued - C::STAGES); i < issued; ++i) {
         const uint32_t bar = smem_u32(&full[i % C::STAGES]);
