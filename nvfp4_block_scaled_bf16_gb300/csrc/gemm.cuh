@@ -127,11 +127,15 @@ struct GemmCfg {
   static constexpr int SF_SLOT = SFA_COLS + SFB_COLS;  // columns of one scale slot
   // a second accumulator only helps CTAs that walk several tiles (epilogue of tile t overlaps
   // the mainloop of t+1)
-  static constexpr int NACC = (MULTI_TILE_ && 2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
+  // (two CTAs per SM share the tensor memory: one accumulator each)
+  static constexpr int NACC = (MULTI_TILE_ && MIN_BLOCKS_ == 1 && 2 * BN + 2 * SF_SLOT <= 512) ? 2 : 1;
   static constexpr int SF_COL0 = NACC * BN;
   // Tensor-memory scale slots: one per ring stage for single-tile (swap-AB) CTAs, so a CTA
   // whose K slice fits the ring writes every stage's scales once, with no slot reuse.
-  static constexpr int SF_SLOTS = !MULTI_TILE_ ? STAGES : (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
+  // (at most one group per ring stage: the writers learn that a group is free from the ring
+  // barrier of the stage that last read it, which is unambiguous only then)
+  static constexpr int SF_SLOTS_FIT = (SF_COL0 + 4 * SF_SLOT <= 512) ? 4 : 2;
+  static constexpr int SF_SLOTS = !MULTI_TILE_ ? STAGES : (SF_SLOTS_FIT < STAGES * SUB ? SF_SLOTS_FIT : STAGES * SUB);
   // The slots of one stage form a group with one written / free barrier pair, so that the MMA
   // lane waits and commits once per stage whatever the number of K steps in it.
   static constexpr int SF_GROUPS = SF_SLOTS / SUB;
@@ -171,6 +175,7 @@ struct GemmCfg {
   static constexpr int SLOT_ARRIVALS = PAIR ? 8 : 4;
   static constexpr int ACC_ARRIVALS = PAIR ? 8 : 4;
   static_assert(TMEM_USED <= 512 && SF_SLOTS <= 8 && SF_SLOTS % SUB == 0, "tensor memory budget, scale-slot barriers");
+  static_assert(SF_GROUPS <= STAGES, "a scale group's reuse is read off the ring barriers: at most one per stage");
   static_assert(STAGES <= 7 && SF_STAGES <= 8 && (2 * STAGES + 46) * 8 + 8 * 4 <= CTRL_BYTES,
                 "barriers and flags fit the control block");
   static_assert(smem_bytes(false) <= 232448, "shared memory per CTA");
@@ -180,7 +185,7 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "MMA N (N = 16 tiles gave wrong results)");
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "128-byte swizzle tiles need 1024-byte alignment");
   static_assert(!PAIR || (MULTI_TILE && BN == 256 && !MX), "CTA pairs: NVFP4 256-wide whole tiles only");
-  static_assert(KS == 1 || (KS == 2 && PAIR), "two K steps per stage: CTA pairs only");
+  static_assert(KS == 1 || (KS == 2 && MULTI_TILE && !MX), "two K steps per stage: NVFP4 multi-tile CTAs only");
 };
 
 struct GemmArgs {

@@ -18,7 +18,18 @@ constexpr int kGroupedBN = 128;
 using GroupedCfg = GemmCfg<kGroupedBN, 6, true>;       // MXFP4: 34 KB stages
 // NVFP4: 36 KB stages; expert tables for up to 512 experts leave room for a 6-deep ring
 using GroupedCfgNv = GemmCfg<kGroupedBN, 6, false, true, 1, false, 512>;
-static_assert(GroupedCfgNv::smem_bytes(true) <= 232448 && GroupedCfg::smem_bytes(true) <= 232448, "smem");
+// NVFP4 with K % 256 == 0: two K steps per 72 KB stage (one 3-D copy per operand), 3 stages
+// (an expert tile's K run is short -- 3 steps at K = 768 -- so per-stage costs weigh)
+using GroupedCfgNv2 = GemmCfg<kGroupedBN, 3, false, true, 1, false, 512, 2>;
+// NVFP4 with at most 256 experts: two CTAs per SM (3-stage rings, one accumulator each), so that
+// one CTA's epilogue overlaps the other's loads and MMAs -- an expert tile's K run is short
+using GroupedCfgNvDuo = GemmCfg<kGroupedBN, 3, false, true, 2, false, 256>;
+using GroupedCfgDuo = GemmCfg<kGroupedBN, 3, true, true, 2, false, 256>;  // (MXFP4)
+static_assert(GroupedCfgNv::smem_bytes(true) <= 232448 && GroupedCfg::smem_bytes(true) <= 232448 &&
+                  GroupedCfgNv2::smem_bytes(true) <= 232448, "smem");
+static_assert(2 * (GroupedCfgNvDuo::smem_bytes(true) + 1024) <= 233472 && 2 * GroupedCfgNvDuo::TMEM_COLS <= 512 &&
+                  2 * (GroupedCfgDuo::smem_bytes(true) + 1024) <= 233472 && 2 * GroupedCfgDuo::TMEM_COLS <= 512,
+              "two CTAs per SM");
 
 // Shared by both grouped entry points: argument checks, tensor maps, launch.
 template <class C>
@@ -47,9 +58,13 @@ nvfp4_status_t grouped_gemm(const char *name, const uint8_t *a, const uint8_t *s
   if (st != NVFP4_OK) return st;
 
   CUtensorMap ta, tb;
-  st = encode_tmap_2d_u8(&ta, a, k / 2, t, k / 2, 128, 128, true);
-  if (st != NVFP4_OK) return st;
-  st = encode_tmap_2d_u8(&tb, b, k / 2, n * num_experts, k / 2, 128, kGroupedBN, true);
+  if constexpr (C::KS == 2) {  // stage views: a box is two 256-wide K steps of 128 rows
+    st = encode_tmap_stages_u8(&ta, a, k / 2, t, 128, 2);
+    if (st == NVFP4_OK) st = encode_tmap_stages_u8(&tb, b, k / 2, n * num_experts, kGroupedBN, 2);
+  } else {
+    st = encode_tmap_2d_u8(&ta, a, k / 2, t, k / 2, 128, 128, true);
+    if (st == NVFP4_OK) st = encode_tmap_2d_u8(&tb, b, k / 2, n * num_experts, k / 2, 128, kGroupedBN, true);
+  }
   if (st != NVFP4_OK) return st;
 
   GemmArgs args{};
@@ -65,7 +80,7 @@ nvfp4_status_t grouped_gemm(const char *name, const uint8_t *a, const uint8_t *s
   args.swap = 0;
   args.m_tiles = 0;
   args.n_tiles = static_cast<int>(ceil_div(n, kGroupedBN));
-  args.k_tiles = static_cast<int>(ceil_div(k, 256));
+  args.k_tiles = static_cast<int>(ceil_div(k, C::KSTAGE));
   args.splits = 1;
   args.sf_chunks = static_cast<int>(round_up(k / C::VEC, 4) / 4);
   args.row_offsets = row_offsets;
@@ -82,7 +97,8 @@ nvfp4_status_t grouped_gemm(const char *name, const uint8_t *a, const uint8_t *s
   auto kern = bs_gemm_kernel<C, true>;
   st = allow_smem(reinterpret_cast<const void *>(kern), C::smem_bytes(true), dev.device);
   if (st != NVFP4_OK) return st;
-  const int grid = static_cast<int>(bound < dev.sm_count ? bound : dev.sm_count);
+  const int slots = C::MIN_BLOCKS * dev.sm_count;
+  const int grid = static_cast<int>(bound < slots ? bound : slots);
   cudaError_t e = launch(kern, dim3(grid), dim3(C::THREADS), C::smem_bytes(true), (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, ta, tb, tb, args);
   return check_launch(e, name);
@@ -94,6 +110,9 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
                                              const uint8_t *b, const uint8_t *sfb,
                                              const float *alpha, void *d, int64_t t, int64_t n,
                                              int64_t k, uint32_t flags, nvfp4_stream_t stream) {
+  if (num_experts <= GroupedCfgDuo::MAX_EXPERTS)
+    return grouped_gemm<GroupedCfgDuo>("mxfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, false,
+                                       d, t, n, k, flags, stream);
   return grouped_gemm<GroupedCfg>("mxfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, false, d, t,
                                   n, k, flags, stream);
 }
@@ -102,6 +121,12 @@ extern "C" nvfp4_status_t nvfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
                                              int num_experts, const uint8_t *b, const uint8_t *sfb,
                                              const float *alpha, void *d, int64_t t, int64_t n, int64_t k,
                                              uint32_t flags, nvfp4_stream_t stream) {
+  if (num_experts <= GroupedCfgNvDuo::MAX_EXPERTS)
+    return grouped_gemm<GroupedCfgNvDuo>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true,
+                                         d, t, n, k, flags, stream);
+  if (k % 256 == 0)
+    return grouped_gemm<GroupedCfgNv2>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true,
+                                       d, t, n, k, flags, stream);
   return grouped_gemm<GroupedCfgNv>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true, d,
                                     t, n, k, flags, stream);
 }
