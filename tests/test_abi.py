@@ -62,12 +62,18 @@ def test_plan_selector_buckets(lib):
     assert lib.nvfp4_gemm_plan(32, 4096, 7168)["tile_n"] == 32
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["tile_n"] == 256
     big = lib.nvfp4_gemm_plan(4096, 4096, 7168)
-    # 256 tiles of 256x256, walked whole and persistently by 76 CTA pairs
+    # 256 tiles of 256x256, walked whole and persistently by 76 CTA pairs; K % 256 == 0, so a
+    # ring stage holds two 256-wide K steps (3 stages)
     assert big["swap_ab"] == 0 and big["tile_m"] == 256 and big["tile_n"] == 256 and big["ctas"] == 152
-    assert big["dp_tiles"] == 256 and big["sk_tiles"] == 0 and big["stages"] == 6
+    assert big["dp_tiles"] == 256 and big["sk_tiles"] == 0 and big["stages"] == 3
     ragged = lib.nvfp4_gemm_plan(300, 13056, 512)           # 3 x 51 single tiles -> 2 x 51 pair tiles
     assert ragged["tile_m"] == 256 and ragged["dp_tiles"] == 102 and ragged["ctas"] == 152
-    assert lib.nvfp4_gemm_plan(1024, 4096, 7168)["tile_m"] == 128   # 128 tiles: 128 x 128, single CTAs
+    # 64 pair tiles fill more than a quarter of the 76 pairs: pairs from 129 tokens on
+    mid = lib.nvfp4_gemm_plan(1024, 4096, 7168)
+    assert mid["tile_m"] == 256 and mid["dp_tiles"] == 64 and mid["ctas"] == 128
+    # 16 pair tiles would fill too few: swap-AB, four-way cluster split-K
+    assert lib.nvfp4_gemm_plan(256, 4096, 7168)["swap_ab"] == 1
+    assert lib.nvfp4_gemm_plan(256, 14336, 4096)["tile_m"] == 256   # 56 pair tiles
     small = lib.nvfp4_gemm_plan(32, 1024, 1024)            # 8 tiles x 4 stages: one stage per CTA
     assert small["splits"] == 4 and small["ctas"] == 32
     few = lib.nvfp4_gemm_plan(640, 1024, 2048)             # 40 tiles but only 2 stages per SM
