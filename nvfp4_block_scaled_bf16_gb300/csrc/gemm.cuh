@@ -1106,6 +1106,30 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       }
     }
   scale_done:;
+    if constexpr (!GROUPED && C::SWAP_ONLY && C::BN >= 64) {
+      // A split tile's partial: the scale writers, idle once the stages are consumed, move the
+      // upper half of the accumulator's columns into the reduction buffer beside the epilogue
+      // warps (each warp reaches the same lane quadrant, warp % 4, as one epilogue warp).
+      Work w2 = work0;
+      Seg sg2;
+      if (p.splits > 1 && w2.next(p, sg2)) {
+        const TileInfo t = tile_info<C, GROUPED>(p, tb, sg2.tile, crank);
+        if (mbar_wait(smem_u32(&accf[0]), 0, wc, kSiteEpilogue)) {
+          tc_fence_after();
+          const int row = (warp & 3) * 32 + lane;
+          float *red = reinterpret_cast<float *>(smem);
+#pragma unroll 1
+          for (int c = C::BN / 64; c < C::BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * c + i < t.cols) red[(32 * c + i) * 128 + row] = __uint_as_float(r[i]);
+          }
+        }
+      }
+    }
   } else if (warp == 10) {
     // ------------------------------------------------------------ scale copies (pairs only)
     // One thread fills the scale ring: both scale slices of each K stage, as far ahead of the
@@ -1180,8 +1204,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       const float tile_alpha = (GROUPED && p.alpha_per_expert && p.alpha) ? __ldg(p.alpha + t.expert) : alpha;
       float *red = reinterpret_cast<float *>(smem);
       float *slot = sk_part ? sk_slot<C>(p, blockIdx.x, sg.j) : nullptr;
+      // (a split swap-AB tile of 64 or more columns: the scale writers take the upper half)
+      const int c_end = (!GROUPED && C::SWAP_ONLY && C::BN >= 64 && p.splits > 1) ? C::BN / 64 : C::BN / 32;
 #pragma unroll 1
-      for (int c = 0; ok && c < C::BN / 32; ++c) {
+      for (int c = 0; ok && c < c_end; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_base + 32 * c, r);
         tmem_ld_wait();
