@@ -621,6 +621,55 @@ __device__ bool quantize_operand_b(const GemmArgs &p, const Tables<C, GROUPED> &
   return true;
 }
 
+// Read form of the cluster split-K reduction: this rank sums the float4 units [u0, u1) of the
+// column-major partials of all p.splits ranks (at red0 in each rank's shared memory).  A thread
+// takes UPT units at a time and issues the distributed-shared-memory loads of every rank's
+// partial for all of them before any sum, so that their latencies overlap.  It then adds each
+// unit in rank order (a fixed order: deterministic output) and writes bf16(alpha * sum).
+template <int UPT, int SMAX>
+__device__ __forceinline__ void reduce_read(const GemmArgs &p, const TileInfo &t, uint32_t red0, int u0, int u1,
+                                            float alpha, int tid, int nt) {
+  for (int ub = u0 + tid; ub < u1; ub += UPT * nt) {
+    float4 part[UPT][SMAX];
+#pragma unroll
+    for (int h = 0; h < UPT; ++h) {
+      const int u = ub + h * nt;
+      const uint32_t off = red0 + static_cast<uint32_t>((u < u1 ? u : ub) * 16);
+#pragma unroll
+      for (int s = 0; s < SMAX; ++s)
+        if (s < p.splits) part[h][s] = ld_cluster_v4(map_to_rank(off, s));
+    }
+#pragma unroll
+    for (int h = 0; h < UPT; ++h) {
+      const int u = ub + h * nt;
+      if (u >= u1) break;
+      float4 v = part[h][0];
+#pragma unroll
+      for (int s = 1; s < SMAX; ++s)
+        if (s < p.splits) {
+          v.x += part[h][s].x;
+          v.y += part[h][s].y;
+          v.z += part[h][s].z;
+          v.w += part[h][s].w;
+        }
+      const int c = (u * 4) / 128, r0 = (u * 4) % 128;
+      if (r0 < t.rows) {
+        const float o[4] = {v.x, v.y, v.z, v.w};
+        if (p.swap) {
+          uint2 pk;
+          pk.x = pack_bf16x2(__fmul_rn(alpha, o[0]), __fmul_rn(alpha, o[1]));
+          pk.y = pack_bf16x2(__fmul_rn(alpha, o[2]), __fmul_rn(alpha, o[3]));
+          *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            p.d[(t.out_i0 + r0 + i) * p.ldd + t.out_j0 + c] = __float2bfloat16_rn(__fmul_rn(alpha, o[i]));
+        }
+      }
+    }
+  }
+}
+
 // Arrive on `bar` once the calling thread's tcgen05 operations so far are complete; for a CTA
 // pair, on the barrier at that offset in both CTAs.
 template <class C>
@@ -1391,9 +1440,7 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
       // Split-K reduction across the cluster.  The partial tile is stored column-major
       // (128 rows per column, a 4-row group per float4 unit); only the units of the tile's
       // valid columns are reduced, CTA `rank` taking a contiguous 1/splits of them.  Every
-      // thread of the CTA takes part, two units at a time: it issues the loads of every rank's
-      // partial for both (independent, so their latencies overlap), then sums each in rank
-      // order (a fixed order: deterministic output).
+      // thread of the CTA takes part, several units at a time (reduce_read).
       cluster_sync();
       {
         const int rank = static_cast<int>(cluster_ctarank());
@@ -1405,46 +1452,10 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         const int units = min(t.cols, C::BN) * 32;  // float4 groups of the valid columns
         const int u0 = rank * units / p.splits, u1 = (rank + 1) * units / p.splits;
         const uint32_t red0 = smem_u32(smem);
-        constexpr int NT = C::THREADS;
-        for (int ub = u0 + static_cast<int>(threadIdx.x); ub < u1; ub += 2 * NT) {
-          float4 part[2][8];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int u = ub + h * NT;
-            const uint32_t off = red0 + static_cast<uint32_t>((u < u1 ? u : ub) * 16);
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-              if (s < p.splits) part[h][s] = ld_cluster_v4(map_to_rank(off, s));
-          }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int u = ub + h * NT;
-            if (u >= u1) break;
-            float4 v = part[h][0];
-#pragma unroll
-            for (int s = 1; s < 8; ++s)
-              if (s < p.splits) {
-                v.x += part[h][s].x;
-                v.y += part[h][s].y;
-                v.z += part[h][s].z;
-                v.w += part[h][s].w;
-              }
-            const int c = (u * 4) / 128, r0 = (u * 4) % 128;
-            if (r0 < t.rows) {
-              const float o[4] = {v.x, v.y, v.z, v.w};
-              if (p.swap) {
-                uint2 pk;
-                pk.x = pack_bf16x2(__fmul_rn(alpha, o[0]), __fmul_rn(alpha, o[1]));
-                pk.y = pack_bf16x2(__fmul_rn(alpha, o[2]), __fmul_rn(alpha, o[3]));
-                *reinterpret_cast<uint2 *>(p.d + (t.out_j0 + c) * p.ldd + t.out_i0 + r0) = pk;
-              } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  p.d[(t.out_i0 + r0 + i) * p.ldd + t.out_j0 + c] = __float2bfloat16_rn(__fmul_rn(alpha, o[i]));
-              }
-            }
-          }
-        }
+        // Two ranks: four units per thread in flight, else two.  (More loads in flight per thread
+        // were measured slower with four ranks: the distributed-shared-memory reads congest.)
+        if (p.splits <= 2) reduce_read<4, 2>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
+        else reduce_read<2, 8>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
       }
       // no CTA leaves while another may still read its partial; those reads are complete here
       // (their sums are stored), so the arrive publishes nothing
