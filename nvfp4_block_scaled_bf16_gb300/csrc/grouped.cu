@@ -21,15 +21,16 @@ using GroupedCfgNv = GemmCfg<kGroupedBN, 6, false, true, 1, false, 512>;
 // NVFP4 with K % 256 == 0: two K steps per 72 KB stage (one 3-D copy per operand), 3 stages
 // (an expert tile's K run is short -- 3 steps at K = 768 -- so per-stage costs weigh)
 using GroupedCfgNv2 = GemmCfg<kGroupedBN, 3, false, true, 1, false, 512, 2>;
-// NVFP4 with at most 256 experts: two CTAs per SM (3-stage rings, one accumulator each), so that
-// one CTA's epilogue overlaps the other's loads and MMAs -- an expert tile's K run is short
-using GroupedCfgNvDuo = GemmCfg<kGroupedBN, 3, false, true, 2, false, 256>;
-using GroupedCfgDuo = GemmCfg<kGroupedBN, 3, true, true, 2, false, 256>;  // (MXFP4)
+// At most 256 experts (tables leave room for a 4-deep ring): 128 x 256 tiles.  Against 128 x 128
+// tiles on two CTAs per SM, an activation tile is read half as often and an MMA does twice the
+// work, which measured 3.5-5 % faster at the MoE shapes (MXFP4 gate+up 85.6 -> 82.2 us, down
+// 65.0 -> 61.6 us; NVFP4 92.7 -> 88.1 and 68.2 -> 65.5 us); a 3-deep ring was slower than both.
+using GroupedCfgWide = GemmCfg<256, 4, true, true, 1, false, 256>;     // MXFP4: 51 KB stages
+using GroupedCfgNvWide = GemmCfg<256, 4, false, true, 1, false, 256>;  // NVFP4: 54 KB stages
 static_assert(GroupedCfgNv::smem_bytes(true) <= 232448 && GroupedCfg::smem_bytes(true) <= 232448 &&
-                  GroupedCfgNv2::smem_bytes(true) <= 232448, "smem");
-static_assert(2 * (GroupedCfgNvDuo::smem_bytes(true) + 1024) <= 233472 && 2 * GroupedCfgNvDuo::TMEM_COLS <= 512 &&
-                  2 * (GroupedCfgDuo::smem_bytes(true) + 1024) <= 233472 && 2 * GroupedCfgDuo::TMEM_COLS <= 512,
-              "two CTAs per SM");
+                  GroupedCfgNv2::smem_bytes(true) <= 232448 && GroupedCfgWide::smem_bytes(true) <= 232448 &&
+                  GroupedCfgNvWide::smem_bytes(true) <= 232448,
+              "smem");
 
 // Shared by both grouped entry points: argument checks, tensor maps, launch.
 template <class C>
@@ -60,10 +61,10 @@ nvfp4_status_t grouped_gemm(const char *name, const uint8_t *a, const uint8_t *s
   CUtensorMap ta, tb;
   if constexpr (C::KS == 2) {  // stage views: a box is two 256-wide K steps of 128 rows
     st = encode_tmap_stages_u8(&ta, a, k / 2, t, 128, 2);
-    if (st == NVFP4_OK) st = encode_tmap_stages_u8(&tb, b, k / 2, n * num_experts, kGroupedBN, 2);
+    if (st == NVFP4_OK) st = encode_tmap_stages_u8(&tb, b, k / 2, n * num_experts, C::BN, 2);
   } else {
     st = encode_tmap_2d_u8(&ta, a, k / 2, t, k / 2, 128, 128, true);
-    if (st == NVFP4_OK) st = encode_tmap_2d_u8(&tb, b, k / 2, n * num_experts, k / 2, 128, kGroupedBN, true);
+    if (st == NVFP4_OK) st = encode_tmap_2d_u8(&tb, b, k / 2, n * num_experts, k / 2, 128, C::BN, true);
   }
   if (st != NVFP4_OK) return st;
 
@@ -79,7 +80,7 @@ nvfp4_status_t grouped_gemm(const char *name, const uint8_t *a, const uint8_t *s
   args.k = static_cast<int>(k);
   args.swap = 0;
   args.m_tiles = 0;
-  args.n_tiles = static_cast<int>(ceil_div(n, kGroupedBN));
+  args.n_tiles = static_cast<int>(ceil_div(n, C::BN));
   args.k_tiles = static_cast<int>(ceil_div(k, C::KSTAGE));
   args.splits = 1;
   args.sf_chunks = static_cast<int>(round_up(k / C::VEC, 4) / 4);
@@ -110,8 +111,8 @@ extern "C" nvfp4_status_t mxfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
                                              const uint8_t *b, const uint8_t *sfb,
                                              const float *alpha, void *d, int64_t t, int64_t n,
                                              int64_t k, uint32_t flags, nvfp4_stream_t stream) {
-  if (num_experts <= GroupedCfgDuo::MAX_EXPERTS)
-    return grouped_gemm<GroupedCfgDuo>("mxfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, false,
+  if (num_experts <= GroupedCfgWide::MAX_EXPERTS)
+    return grouped_gemm<GroupedCfgWide>("mxfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, false,
                                        d, t, n, k, flags, stream);
   return grouped_gemm<GroupedCfg>("mxfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, false, d, t,
                                   n, k, flags, stream);
@@ -121,8 +122,8 @@ extern "C" nvfp4_status_t nvfp4_grouped_gemm(const uint8_t *a, const uint8_t *sf
                                              int num_experts, const uint8_t *b, const uint8_t *sfb,
                                              const float *alpha, void *d, int64_t t, int64_t n, int64_t k,
                                              uint32_t flags, nvfp4_stream_t stream) {
-  if (num_experts <= GroupedCfgNvDuo::MAX_EXPERTS)
-    return grouped_gemm<GroupedCfgNvDuo>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true,
+  if (num_experts <= GroupedCfgNvWide::MAX_EXPERTS)
+    return grouped_gemm<GroupedCfgNvWide>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true,
                                          d, t, n, k, flags, stream);
   if (k % 256 == 0)
     return grouped_gemm<GroupedCfgNv2>("nvfp4_grouped_gemm", a, sfa, row_offsets, num_experts, b, sfb, alpha, true,
