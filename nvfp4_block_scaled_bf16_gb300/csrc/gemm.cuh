@@ -1452,10 +1452,18 @@ __global__ void __launch_bounds__(C::THREADS, C::MIN_BLOCKS)
         const int units = min(t.cols, C::BN) * 32;  // float4 groups of the valid columns
         const int u0 = rank * units / p.splits, u1 = (rank + 1) * units / p.splits;
         const uint32_t red0 = smem_u32(smem);
-        // Two ranks: four units per thread in flight, else two.  (More loads in flight per thread
-        // were measured slower with four ranks: the distributed-shared-memory reads congest.)
-        if (p.splits <= 2) reduce_read<4, 2>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
-        else reduce_read<2, 8>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
+        // Two ranks of a 128- or 256-wide tile: four units per thread in flight, else two.  (More
+        // loads in flight per thread were measured slower with four ranks: the distributed
+        // shared-memory reads congest.  The narrower tiles keep one form, whose code measured
+        // faster there.)
+        bool done = false;
+        if constexpr (C::BN >= 128) {
+          if (p.splits <= 2) {
+            reduce_read<4, 2>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
+            done = true;
+          }
+        }
+        if (!done) reduce_read<2, 8>(p, t, red0, u0, u1, alpha, static_cast<int>(threadIdx.x), C::THREADS);
       }
       // no CTA leaves while another may still read its partial; those reads are complete here
       // (their sums are stored), so the arrive publishes nothing
