@@ -357,6 +357,95 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
   }
 }
 
+// The same quantisation with one thread per (scale row, scale column) position of the grouped
+// padded scale matrix: consecutive threads take consecutive 16-element blocks, so a warp's loads
+// are contiguous even where a row has few blocks (48 at K = 768), no lane idles on a partial
+// pass, and each thread looks up the expert of its scale row in shared memory (a warp's lanes
+// read the same entries).  The scale-row prefix is a warp scan.  32-bit positions, rows and
+// offsets: the host launches it only when rows * columns < 2^31 (so t < 2^31 too).
+// Measured at 128 experts, 32768 rows: SiLU form 67.5 -> 49.2 us, plain form (K=2048) 45.4 ->
+// 38.9 us against the warp-per-row kernel, bit-identical.
+template <bool SILU>
+__global__ void __launch_bounds__(256) expert_quant_pos_kernel(const __nv_bfloat16 *__restrict__ x, int64_t t,
+                                                               int kb, int64_t ldx, int64_t up_off,
+                                                               const int64_t *__restrict__ row_offsets,
+                                                               int experts, const float *__restrict__ gs_e,
+                                                               uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
+                                                               int64_t cap_rows, int cp) {
+  __shared__ int s_ro[kMaxExpertsMoe + 1];
+  __shared__ int s_sfr[kMaxExpertsMoe + 1];
+  pdl_trigger();
+  pdl_wait();
+  for (int e = threadIdx.x; e <= experts; e += blockDim.x) s_ro[e] = static_cast<int>(row_offsets[e]);
+  __syncthreads();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < experts; base += 32) {
+      const int e = base + lane;
+      int v = 0;
+      if (e < experts) {
+        const int cnt = s_ro[e + 1] - s_ro[e];
+        v = (cnt > 0 ? cnt + 127 : 0) / 128 * 128;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += n;
+      }
+      if (e < experts) s_sfr[e + 1] = carry + v;
+      carry += __shfl_sync(0xFFFFFFFFu, v, 31);
+    }
+    if (lane == 0) s_sfr[0] = 0;
+  }
+  __syncthreads();
+  const int rows = static_cast<int>(s_sfr[experts] < cap_rows ? s_sfr[experts] : cap_rows);
+  const int total = rows * cp;  // a multiple of 512: every warp runs the same trip count
+  const int stride = gridDim.x * blockDim.x;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int srow = idx / cp, j = idx - srow * cp;
+    int lo = 0, hi = experts - 1;  // expert owning scale row srow: largest e with s_sfr[e] <= srow
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_sfr[mid] <= srow) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t local = srow - s_sfr[lo];
+    const int64_t r = s_ro[lo] + local;
+    const bool row_ok = local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t;
+    uint32_t code = 0;
+    if (row_ok && j < kb) {
+      const float gs = __ldg(gs_e + lo);
+      const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
+      const uint4 g0 = __ldg(src), g1 = __ldg(src + 1);
+      uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
+      if (SILU) {
+        const uint4 *up = reinterpret_cast<const uint4 *>(x + r * ldx + up_off + j * 16);
+        u0 = __ldg(up);
+        u1 = __ldg(up + 1);
+      }
+      float f[16];
+      bf16x8_to_f32_moe(g0, f);
+      bf16x8_to_f32_moe(g1, f + 8);
+      if (SILU) {
+        float u[16];
+        bf16x8_to_f32_moe(u0, u);
+        bf16x8_to_f32_moe(u1, u + 8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) silu_mul_bf16x2(f[2 * i], f[2 * i + 1], u[2 * i], u[2 * i + 1]);
+      }
+      *reinterpret_cast<uint2 *>(q + r * (static_cast<int64_t>(kb) * 8) + j * 8) = nvfp4_block16(f, gs, code);
+    }
+    // 4 lanes (scale columns 4c .. 4c+3 of the row) -> one 32-bit word of the 128x4 layout
+    const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+    const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
+    const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+    if ((j & 3) == 0)
+      *reinterpret_cast<uint32_t *>(sf + static_cast<int64_t>(srow >> 7) * (cp >> 2) * 512 + (srow & 31) * 16 +
+                                    ((srow >> 5) & 3) * 4 + (j >> 2) * 512) = code | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+}
+
 // CTAs of the two sort kernels: about 32 tokens each, at most 1024 (the workspace holds one
 // count per CTA and expert).
 int moe_sort_ctas(int64_t tokens) {
@@ -459,6 +548,11 @@ extern "C" nvfp4_status_t moe_combine(const void *y, int64_t rows, const int32_t
 }
 
 namespace {
+// Which per-expert quantiser runs (positions: one thread per scale position; else one warp per
+// scale row), and how many 256-thread blocks per SM the position form launches at most.
+constexpr bool kPosQuant = true;
+constexpr int kPosQuantBlocksPerSm = 16;
+
 nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t t, int64_t k, int64_t ldx,
                             const int64_t *row_offsets, int num_experts, const float *gs, uint8_t *q, uint8_t *sf,
                             size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream) {
@@ -484,6 +578,16 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
   if (st != NVFP4_OK) return st;
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
   const int64_t scale_rows = round_up(t, 128) + 128LL * num_experts;  // bound of sum_e round_up(M_e, 128)
+  if (kPosQuant && scale_rows * cp < (1LL << 31)) {
+    auto kern = silu ? expert_quant_pos_kernel<true> : expert_quant_pos_kernel<false>;
+    const int64_t blocks = ceil_div(scale_rows * cp, 256);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * kPosQuantBlocksPerSm;
+    cudaError_t e = launch(kern, dim3(static_cast<int>(blocks < cap ? blocks : cap)), dim3(256), 0,
+                           (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x),
+                           t, static_cast<int>(k / 16), ldx, silu ? k : static_cast<int64_t>(0), row_offsets, num_experts,
+                           gs, q, sf, cap_rows, static_cast<int>(cp));
+    return check_launch(e, name);
+  }
   auto kern = silu ? expert_quant_kernel<true> : expert_quant_kernel<false>;
   cudaError_t e = launch(kern, dim3(moe_grid(scale_rows * 32, dev.sm_count)), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x), t,
