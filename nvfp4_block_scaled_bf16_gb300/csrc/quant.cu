@@ -48,24 +48,25 @@ __device__ __forceinline__ uint32_t gather4(uint32_t code) {
 }
 
 // total = round_up(m,128) * cp, a multiple of 512, so every warp runs the same trip count.
-// SM103: scales in the SM103 layout instead of the 128x4 one.
-template <bool SM103>
+// SM103: scales in the SM103 layout instead of the 128x4 one.  I: the position type (32-bit
+// when total < 2^31: its division is several times cheaper than the 64-bit one).
+template <bool SM103, typename I>
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                           int64_t m, int64_t kb, int64_t ldx,
                                                           const float *__restrict__ gs_ptr,
                                                           uint8_t *__restrict__ q,
-                                                          uint8_t *__restrict__ sf, int64_t total,
-                                                          int64_t cp) {
+                                                          uint8_t *__restrict__ sf, int64_t total_,
+                                                          int64_t cp_) {
+  const I total = static_cast<I>(total_), cp = static_cast<I>(cp_);
   // Let the next kernel launch at once (it waits for this grid's completion before it reads
   // our outputs), then wait for our own predecessor before reading x.
   pdl_trigger();
   pdl_wait();
   const float gs = __ldg(gs_ptr);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
     const int64_t r = idx / cp;
-    const int64_t j = idx - r * cp;
+    const int64_t j = idx - static_cast<I>(r) * cp;
     uint32_t code = 0;
     if (r < m && j < kb) {
       const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
@@ -82,6 +83,7 @@ constexpr int kMaxExperts = 1024;
 
 // Scale rows of the (optionally expert-grouped) MXFP4 layout: expert e owns scale rows
 // sfr[e] .. sfr[e+1]-1, sfr[e+1] - sfr[e] = round_up(M_e, 128).
+template <typename I>
 __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                           int64_t t, int64_t kb, int64_t ldx,
                                                           const int64_t *__restrict__ row_offsets,
@@ -105,25 +107,34 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
   } else {
     for (int e = threadIdx.x; e <= experts; e += blockDim.x) s_ro[e] = row_offsets[e];
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int64_t acc = 0;
-      s_sfr[0] = 0;
-      for (int e = 0; e < experts; ++e) {
-        int64_t cnt = s_ro[e + 1] - s_ro[e];
-        cnt = cnt < 0 ? 0 : cnt;
-        acc += (cnt + 127) / 128 * 128;
-        s_sfr[e + 1] = acc;
+    if (threadIdx.x < 32) {  // scale-row prefix: a warp scan over the experts, 32 at a time
+      const int lane = threadIdx.x;
+      int64_t carry = 0;
+      for (int base = 0; base < experts; base += 32) {
+        const int e = base + lane;
+        int64_t v = 0;
+        if (e < experts) {
+          const int64_t cnt = s_ro[e + 1] - s_ro[e];
+          v = (cnt > 0 ? cnt + 127 : 0) / 128 * 128;
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int64_t n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+          if (lane >= o) v += n;
+        }
+        if (e < experts) s_sfr[e + 1] = carry + v;
+        carry += __shfl_sync(0xFFFFFFFFu, v, 31);
       }
+      if (lane == 0) s_sfr[0] = 0;
     }
   }
   __syncthreads();
   const int64_t rows = s_sfr[experts] < cap_rows ? s_sfr[experts] : cap_rows;
-  const int64_t total = rows * cp;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    const int64_t s = idx / cp;
-    const int64_t j = idx - s * cp;
+  const I total = static_cast<I>(rows * cp), cpi = static_cast<I>(cp);
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int64_t s = idx / cpi;
+    const int64_t j = idx - static_cast<I>(s) * cpi;
     // expert owning scale row s: the largest e with s_sfr[e] <= s
     int lo = 0, hi = experts - 1;
     while (lo < hi) {
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
 
 int quant_grid(int64_t total_threads, int sm_count) {
   const int64_t blocks = ceil_div(total_threads, 256);
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  const int64_t cap = static_cast<int64_t>(sm_count) * 16;
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
@@ -190,7 +201,9 @@ extern "C" nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, in
   const int64_t cp = round_up(k / 16, 4);
   const int64_t total = round_up(m, 128) * cp;
   const int grid = quant_grid(total, dev.sm_count);
-  auto kern = (flags & NVFP4_FLAG_SF_SM103) ? nvfp4_quant_kernel<true> : nvfp4_quant_kernel<false>;
+  const bool narrow = total < (1LL << 31);
+  auto kern = (flags & NVFP4_FLAG_SF_SM103) ? (narrow ? nvfp4_quant_kernel<true, int> : nvfp4_quant_kernel<true, int64_t>)
+                                            : (narrow ? nvfp4_quant_kernel<false, int> : nvfp4_quant_kernel<false, int64_t>);
   cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, m, k / 16,
                          ldx, gs, q, sf, total, cp);
@@ -223,7 +236,9 @@ extern "C" nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, in
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
   const int64_t total = (row_offsets ? round_up(t, 128) + 128LL * num_experts : round_up(t, 128)) * cp;
   const int grid = quant_grid(total, dev.sm_count);
-  cudaError_t e = launch(mxfp4_quant_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+  // (the kernel's positions cover at most `total`: 32-bit when that fits)
+  auto kern = total < (1LL << 31) ? mxfp4_quant_kernel<int> : mxfp4_quant_kernel<int64_t>;
+  cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, t, k / 32,
                          ldx, row_offsets, row_offsets ? num_experts : 1, q, sf, cap_rows, cp);
   return check_launch(e, "mxfp4_quantize");
