@@ -126,16 +126,20 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) moe_place_kernel(const int32
 // ------------------------------------------------------------------ row gather
 // out[r, :] = x[src[r], :] for r < rows; 16-byte pieces, grid-stride.  A source row outside
 // [0, T) sets bit 3 of the status word and its output row is left untouched.
+// I: the position type (32-bit when rows * pieces < 2^31: a cheaper division per position).
+template <typename I>
 __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict__ x, int64_t ldx16, int64_t T,
                                                          const int32_t *__restrict__ src, int64_t rows,
-                                                         int64_t pieces, uint4 *__restrict__ out,
+                                                         int64_t pieces_, uint4 *__restrict__ out,
                                                          unsigned int *status) {
   pdl_trigger();
   pdl_wait();
-  const int64_t total = rows * pieces;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t r = i / pieces, c = i - r * pieces;
+  const I pieces = static_cast<I>(pieces_);
+  const I total = static_cast<I>(rows * pieces_);
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I i = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const I r_ = i / pieces;
+    const int64_t r = r_, c = i - r_ * pieces;
     const int64_t s = src[r];
     if (s < 0 || s >= T) {
       if (c == 0) atomicOr(status, 8u);
@@ -149,17 +153,21 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict
 // out[t, :] = bf16(sum_j w[t, j] * y[pos[t, j], :]), fp32 products and sums in slot order, no
 // fused multiply-add; a slot with pos < 0 (an entry the sort dropped) contributes nothing.
 // One thread per 8 output elements (16-byte loads of y, 16-byte store).
+// I: the position type (as in the gather).
+template <typename I>
 __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4 *__restrict__ y, int64_t rows,
                                                           const int32_t *__restrict__ pos,
                                                           const float *__restrict__ w, int64_t T, int topk,
-                                                          int64_t pieces, uint4 *__restrict__ out,
+                                                          int64_t pieces_, uint4 *__restrict__ out,
                                                           unsigned int *status) {
   pdl_trigger();
   pdl_wait();
-  const int64_t total = T * pieces;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-    const int64_t t = i / pieces, c = i - t * pieces;
+  const I pieces = static_cast<I>(pieces_);
+  const I total = static_cast<I>(T * pieces_);
+  const I stride = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I i = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const I t_ = i / pieces;
+    const int64_t t = t_, c = i - t_ * pieces;
     float acc[8];
     bool first = true;
     for (int j = 0; j < topk; ++j) {
@@ -453,11 +461,13 @@ int moe_sort_ctas(int64_t tokens) {
   return static_cast<int>(g < 1024 ? g : 1024);
 }
 
-int moe_grid(int64_t threads, int sm_count) {
+int moe_grid(int64_t threads, int sm_count, int per_sm = 8) {
   const int64_t blocks = ceil_div(threads, 256);
-  const int64_t cap = static_cast<int64_t>(sm_count) * 8;
+  const int64_t cap = static_cast<int64_t>(sm_count) * per_sm;
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
+// blocks per SM the gather and combine launch at most
+constexpr int kMoveBlocksPerSm = 8;
 
 }  // namespace
 }  // namespace nvfp4
@@ -519,7 +529,8 @@ extern "C" nvfp4_status_t moe_gather_rows(const void *x, int64_t num_tokens, int
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   const int64_t pieces = h / 8;
-  cudaError_t e = launch(moe_gather_kernel, dim3(moe_grid(rows * pieces, dev.sm_count)), dim3(256), 0,
+  auto kern = rows * pieces < (1LL << 31) ? moe_gather_kernel<int> : moe_gather_kernel<int64_t>;
+  cudaError_t e = launch(kern, dim3(moe_grid(rows * pieces, dev.sm_count, kMoveBlocksPerSm)), dim3(256), 0,
                          (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(x),
                          ldx / 8, num_tokens, src_rows, rows, pieces, static_cast<uint4 *>(out), dev.status);
   return check_launch(e, "moe_gather_rows");
@@ -541,7 +552,9 @@ extern "C" nvfp4_status_t moe_combine(const void *y, int64_t rows, const int32_t
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   const int64_t pieces = h / 8;
-  cudaError_t e = launch(moe_combine_kernel, dim3(moe_grid(num_tokens * pieces, dev.sm_count)), dim3(256), 0,
+  const bool narrow = num_tokens * pieces < (1LL << 31);
+  auto kern = narrow ? moe_combine_kernel<int> : moe_combine_kernel<int64_t>;
+  cudaError_t e = launch(kern, dim3(moe_grid(num_tokens * pieces, dev.sm_count, kMoveBlocksPerSm)), dim3(256), 0,
                          (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(y), rows,
                          pos, weights, num_tokens, topk, pieces, static_cast<uint4 *>(out), dev.status);
   return check_launch(e, "moe_combine");
