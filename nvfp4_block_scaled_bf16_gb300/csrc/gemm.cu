@@ -229,6 +229,11 @@ nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, 
   if (st != NVFP4_OK) return st;
 
   const Plan pl = select_plan(m, n, k, dev.sm_count);
+  // A swap-AB plan holds every token in one tile (tile_n >= m): the kernels read operand B's
+  // scales with scale-factor ID 0, i.e. rows 0..BN-1 of each 128-row scale block, so a second
+  // token tile at a row offset that is not a multiple of 128 would take the wrong scales.
+  if (pl.swap && pl.n_tiles != 1)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: internal plan error (swap-AB with %d token tiles)", name, pl.n_tiles);
   if (fused && !pl.swap)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "%s: the quantisation is fused into the weight-streaming plans (m <= 256, got %lld); quantise with "

@@ -90,6 +90,16 @@ def test_plan_selector_buckets(lib):
         assert p["dp_tiles"] + p["sk_tiles"] == tiles
 
 
+def test_swap_plans_hold_every_token_in_one_tile(lib):
+    """The swap-AB kernels read operand B's scales at scale-factor ID 0 (rows 0..tile_n-1 of a
+    128-row scale block), so a swap plan must cover all M tokens with one tile."""
+    for m in list(range(1, 40)) + [48, 63, 64, 65, 96, 127, 128, 129, 192, 255, 256]:
+        for (n, k) in ((4096, 7168), (7168, 2048), (14336, 4096), (1024, 1024)):
+            p = lib.nvfp4_gemm_plan(m, n, k)
+            if p["swap_ab"]:
+                assert p["tile_n"] >= m, (m, n, k, p)
+
+
 def test_workspace_size(lib):
     """Counters (one per split tile, padded to 256 B) + 2 fp32 slots of 128 x tile_n per CTA."""
     assert lib.gemm_workspace_size(1, 4096, 7168) == 0        # cluster split-K needs none
