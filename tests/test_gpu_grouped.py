@@ -62,6 +62,12 @@ def test_alpha_and_k_tail(nv):
     _check(nv, [5, 200, 64], 128, 96 * 2, alpha=0.25)
 
 
+def test_ragged_n_tiles(nv):
+    """N = 288: each expert's 256-wide column tile and a 32-wide one (B rows past the expert's
+    last belong to the next expert, their columns are not stored)."""
+    _check(nv, [40, 0, 170, 7], 288, 256)
+
+
 def test_largest_expert_count(nv):
     """1024 experts (the MXFP4 grouped GEMM's limit), most with 0..3 rows."""
     counts = np.random.default_rng(4).integers(0, 4, 1024).tolist()

@@ -118,6 +118,7 @@ def _expert_weights(E, N, K, seed):
 
 @pytest.mark.parametrize("counts,N,K", [([3, 0, 40], 64, 128), ([0, 130, 1, 257], 256, 512),
                                         ([5, 0, 131, 260], 192, 768),  # two K steps per stage, the last half
+                                        ([7, 129, 0, 64], 288, 256),   # a 256-wide tile and a 32-wide one
                                         (list(np.random.default_rng(2).integers(0, 300, 16)), 1536, 2048),
                                         (list(np.random.default_rng(3).integers(0, 4, 512)), 64, 128)])
 def test_nvfp4_grouped_gemm(nv, counts, N, K):
