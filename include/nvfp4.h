@@ -319,7 +319,8 @@ nvfp4_status_t nvfp4_silu_mul_quantize_experts(const void *x, int64_t t, int64_t
  *   b      uint8 [num_experts, n, k/2];  sfb  uint8 [num_experts, nvfp4_sf_bytes(n, k, 16)]
  *   alpha  DEVICE fp32 [num_experts] (one per expert: 1/(gsA_e * gsB_e)) or NULL for 1.0
  *   d      bf16 [t, n], 32-B aligned;  n % 32 == 0, k % 32 == 0;  1 <= num_experts <= 512 (the
- *          expert tables share the CTA's shared memory with a 6-deep operand ring).
+ *          expert tables share the CTA's shared memory with the operand ring: 128 x 256 tiles on a
+ *          4-deep ring up to 256 experts, 128 x 128 tiles beyond).
  * Same kernel, other checks and PDL behaviour as mxfp4_grouped_gemm. */
 nvfp4_status_t nvfp4_grouped_gemm(const uint8_t *a, const uint8_t *sfa, const int64_t *row_offsets, int num_experts,
                                   const uint8_t *b, const uint8_t *sfb, const float *alpha, void *d, int64_t t,
