@@ -342,8 +342,8 @@ def nvfp4_grouped_bytes(experts, t, n, k):
 
 
 def make_moe_nvfp4(nv):
-    """A whole NVFP4 MoE layer (the f3 steps): sort -> gather -> quantise -> gate+up grouped GEMM
-    -> SiLU*mul + quantise -> down grouped GEMM -> combine, chained with PDL.  128 experts, 4096
+    """A whole NVFP4 MoE layer (the f3 steps): sort -> gather + quantise (one kernel) -> gate+up
+    grouped GEMM -> SiLU*mul + quantise -> down grouped GEMM -> combine, chained with PDL.  128 experts, 4096
     tokens top-8, hidden 2048, expert intermediate 768 (the MXFP4 MoE shape, NVFP4 formats)."""
     wl = Workload(nv, "moe_nvfp4")
     E, T, topk, H, I = 128, 4096, 8, 2048, 768
@@ -366,7 +366,6 @@ def make_moe_nvfp4(nv):
     ro = torch.empty(E + 1, dtype=torch.int64, device="cuda")
     src = torch.empty(R, dtype=torch.int32, device="cuda")
     pos = torch.empty((T, topk), dtype=torch.int32, device="cuda")
-    xg = torch.empty((R, H), dtype=torch.bfloat16, device="cuda")
     q1 = torch.empty((R, H // 2), dtype=torch.uint8, device="cuda")
     s1 = torch.empty(nv.expert_sf_bytes(R, E, H), dtype=torch.uint8, device="cuda")
     h1 = torch.empty((R, 2 * I), dtype=torch.bfloat16, device="cuda")
@@ -388,8 +387,7 @@ def make_moe_nvfp4(nv):
     L = wl.launches
     sort_ws = torch.empty(max(1, nv.moe_sort_workspace_size(T, E) // 4), dtype=torch.int32, device="cuda")
     L.append(lambda: nv.moe_sort_by_expert(ids_d, E, out=(ro, src, pos), workspace=sort_ws, flags=P))
-    L.append(lambda: nv.moe_gather_rows(xd, src, out=xg, flags=P))
-    L.append(lambda: nv.nvfp4_quantize_experts(xg, ro, gs1, q=q1, sf=s1, flags=P))
+    L.append(lambda: nv.nvfp4_gather_quantize_experts(xd, src, ro, gs1, q=q1, sf=s1, flags=P))
     g1 = (lambda: nv.nvfp4_grouped_gemm(q1, s1, ro, specs["gate_up"][0], specs["gate_up"][1], a1, d=h1, flags=P))
     L.append(g1)
     L.append(lambda: nv.nvfp4_silu_mul_quantize_experts(h1, ro, gs2, q=q2, sf=s2, flags=P))
@@ -401,10 +399,10 @@ def make_moe_nvfp4(nv):
     wl.gemm_bytes = nvfp4_grouped_bytes(E, R, 2 * I, H) + nvfp4_grouped_bytes(E, R, H, I)
     wl.quant_bytes = quant_bytes(R, H) + quant_bytes(R, 2 * I)
     wl.h2d += [(xd, x.pin_memory()), (ids_d, ids.pin_memory()), (wts_d, wts.pin_memory())]
-    wl.h2d_at += [1, 0, 6]                               # gather, sort, combine
+    wl.h2d_at += [1, 0, 5]                               # gather+quantise, sort, combine
     wl.d2h.append((torch.empty((T, H), dtype=torch.bfloat16).pin_memory(), out))
     wl.config = {"workload": "NVFP4 MoE layer: 128 experts, 4096 tokens top-8 (32768 rows), hidden 2048, intermediate "
-                             "768; sort, gather, quantise, gate+up grouped GEMM (N=1536, K=2048), SiLU*mul+quantise, "
+                             "768; sort, gather+quantise, gate+up grouped GEMM (N=1536, K=2048), SiLU*mul+quantise, "
                              "down grouped GEMM (N=2048, K=768), combine",
                  "global_batch": R, "inputs": "activation N(0,1), expert weights N(0,0.02), router logits N(0,1), seed 0",
                  "l2": "flushed before every timed step (512 MB write, then 512 MB read)", "parallelism": "replicas"}

@@ -11,6 +11,7 @@
  *   sf_swizzle          row-major scale matrix <-> 128x4 swizzled layout
  *   nvfp4_sf_convert_layout  128x4 ("SM100") <-> SM103 scale layout
  *   MoE steps           moe_sort_by_expert, moe_gather_rows, nvfp4_quantize_experts,
+ *                       nvfp4_gather_quantize_experts (the two fused),
  *                       nvfp4_silu_mul_quantize_experts, nvfp4_grouped_gemm, moe_combine
  *   sizes and status    nvfp4_sf_bytes, mxfp4_grouped_sf_bytes, moe_sort_workspace_size,
  *                       nvfp4_check_status, nvfp4_last_error
@@ -301,6 +302,23 @@ nvfp4_status_t moe_gather_rows(const void *x, int64_t num_tokens, int64_t h, int
 nvfp4_status_t nvfp4_quantize_experts(const void *x, int64_t t, int64_t k, int64_t ldx, const int64_t *row_offsets,
                                       int num_experts, const float *gs, uint8_t *q, uint8_t *sf, size_t sf_bytes,
                                       uint32_t flags, nvfp4_stream_t stream);
+
+/* moe_gather_rows fused into nvfp4_quantize_experts: row r of the quantised matrix is row
+ * src_rows[r] of x, so the gathered bf16 copy is never written.  For src_rows entries in
+ * [0, num_tokens) the result (q, sf) is bit-identical to moe_gather_rows(x, src_rows) followed
+ * by nvfp4_quantize_experts on its output.  A row whose entry is outside [0, num_tokens) is
+ * quantised from zeros and makes nvfp4_check_status report NVFP4_ERR_INVALID_ARG.  The sources
+ * define no such call: it joins two of the steps above ([vLLM-SM103] ops.h quantises the
+ * already permuted activation with scaled_fp4_experts_quant).
+ *   x         bf16 [num_tokens, k], row stride ldx >= k (ldx % 8 == 0), 16-B aligned
+ *   src_rows  DEVICE int32 [rows] (as moe_sort_by_expert writes it), 4-B aligned
+ *   row_offsets, num_experts, gs, q ([rows, k/2]), sf, sf_bytes: as nvfp4_quantize_experts
+ *   with t = rows.  (rows + 128*num_experts) * round_up(k/16,4) < 2^31, else
+ *   NVFP4_ERR_UNSUPPORTED_SHAPE (quantise the gathered rows with nvfp4_quantize_experts). */
+nvfp4_status_t nvfp4_gather_quantize_experts(const void *x, int64_t num_tokens, int64_t k, int64_t ldx,
+                                             const int32_t *src_rows, int64_t rows, const int64_t *row_offsets,
+                                             int num_experts, const float *gs, uint8_t *q, uint8_t *sf,
+                                             size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream);
 
 /* SiLU-and-mul fused with the per-expert NVFP4 quantisation (silu_and_mul_scaled_fp4_experts_quant).
  * x is bf16 [t, 2*inter] = [gate | up]; the quantised matrix is h [t, inter] with

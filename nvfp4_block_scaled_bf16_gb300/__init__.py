@@ -54,6 +54,8 @@ _SIGS = {
     "moe_sort_by_expert": (_int, [_vp, _i64, _int, _int, _vp, _vp, _vp, _vp, _sz, _u32, _vp]),
     "moe_gather_rows": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _u32, _vp]),
     "nvfp4_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
+    "nvfp4_gather_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32,
+                                             _vp]),
     "nvfp4_silu_mul_quantize_experts": (_int, [_vp, _i64, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u32, _vp]),
     "nvfp4_grouped_gemm": (_int, [_vp, _vp, _vp, _int, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _u32, _vp]),
     "moe_combine": (_int, [_vp, _i64, _vp, _vp, _i64, _int, _i64, _vp, _u32, _vp]),
@@ -411,6 +413,33 @@ def nvfp4_quantize_experts(x, row_offsets, gs, q=None, sf=None, flags: int = 0, 
     _room(sf, torch.uint8, "sf", 0)            # its capacity goes to the library, which checks it
     _check(_lib.nvfp4_quantize_experts(_ptr(x), t, k, x.stride(0), _ptr(row_offsets), experts, _ptr(gs), _ptr(q),
                                        _ptr(sf), sf.numel(), flags, _stream(stream)))
+    return q, sf
+
+
+def nvfp4_gather_quantize_experts(x, src_rows, row_offsets, gs, q=None, sf=None, flags: int = 0, stream=None):
+    """Row r of the result quantises x[src_rows[r]]: moe_gather_rows + nvfp4_quantize_experts in one launch."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(src_rows, torch.int32, "src_rows", 1)
+    _need(row_offsets, torch.int64, "row_offsets", 1)
+    _need(gs, torch.float32, "gs", 1)
+    if x.stride(1) != 1:
+        raise ValueError("x rows must be contiguous")
+    if not src_rows.is_contiguous():
+        raise ValueError("src_rows must be contiguous")
+    tokens, k = x.shape
+    rows = src_rows.numel()
+    experts = row_offsets.numel() - 1
+    if q is None:
+        q = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    if sf is None:
+        sf = torch.empty(expert_sf_bytes(rows, experts, k), dtype=torch.uint8, device=x.device)
+    _room(row_offsets, torch.int64, "row_offsets", experts + 1)
+    _room(gs, torch.float32, "gs", experts)
+    _room(q, torch.uint8, "q", rows * (k // 2))
+    _room(sf, torch.uint8, "sf", 0)            # its capacity goes to the library, which checks it
+    _check(_lib.nvfp4_gather_quantize_experts(_ptr(x), tokens, k, x.stride(0), _ptr(src_rows), rows,
+                                              _ptr(row_offsets), experts, _ptr(gs), _ptr(q), _ptr(sf), sf.numel(),
+                                              flags, _stream(stream)))
     return q, sf
 
 

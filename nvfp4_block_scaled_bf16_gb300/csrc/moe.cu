@@ -373,13 +373,15 @@ __global__ void __launch_bounds__(256) expert_quant_kernel(const __nv_bfloat16 *
 // offsets: the host launches it only when rows * columns < 2^31 (so t < 2^31 too).
 // Measured at 128 experts, 32768 rows: SiLU form 67.5 -> 49.2 us, plain form (K=2048) 45.4 ->
 // 38.9 us against the warp-per-row kernel, bit-identical.
-template <bool SILU>
+template <bool SILU, bool GATHER>
 __global__ void __launch_bounds__(256) expert_quant_pos_kernel(const __nv_bfloat16 *__restrict__ x, int64_t t,
                                                                int kb, int64_t ldx, int64_t up_off,
                                                                const int64_t *__restrict__ row_offsets,
                                                                int experts, const float *__restrict__ gs_e,
                                                                uint8_t *__restrict__ q, uint8_t *__restrict__ sf,
-                                                               int64_t cap_rows, int cp) {
+                                                               int64_t cap_rows, int cp,
+                                                               const int32_t *__restrict__ src, int64_t tokens,
+                                                               unsigned int *status) {
   __shared__ int s_ro[kMaxExpertsMoe + 1];
   __shared__ int s_sfr[kMaxExpertsMoe + 1];
   pdl_trigger();
@@ -420,15 +422,30 @@ __global__ void __launch_bounds__(256) expert_quant_pos_kernel(const __nv_bfloat
     }
     const int64_t local = srow - s_sfr[lo];
     const int64_t r = s_ro[lo] + local;
-    const bool row_ok = local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t;
+    bool row_ok = local < s_ro[lo + 1] - s_ro[lo] && r >= 0 && r < t;
+    // GATHER: row r of the quantised matrix is row src[r] of x (moe_gather_rows fused in); a
+    // source outside [0, tokens) quantises zeros and sets bit 3 of the status word
+    int64_t xr = r;
+    bool zero_row = false;  // GATHER: a row of the result whose source is out of range
+    if (GATHER && row_ok) {
+      xr = src[r];
+      if (xr < 0 || xr >= tokens) {
+        if (j == 0) atomicOr(status, 8u);
+        zero_row = true;
+      }
+    }
     uint32_t code = 0;
     if (row_ok && j < kb) {
       const float gs = __ldg(gs_e + lo);
-      const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
-      const uint4 g0 = __ldg(src), g1 = __ldg(src + 1);
+      const uint4 *xs = reinterpret_cast<const uint4 *>(x + xr * ldx + j * 16);
+      uint4 g0 = make_uint4(0u, 0u, 0u, 0u), g1 = g0;
+      if (!zero_row) {
+        g0 = __ldg(xs);
+        g1 = __ldg(xs + 1);
+      }
       uint4 u0 = make_uint4(0u, 0u, 0u, 0u), u1 = u0;
       if (SILU) {
-        const uint4 *up = reinterpret_cast<const uint4 *>(x + r * ldx + up_off + j * 16);
+        const uint4 *up = reinterpret_cast<const uint4 *>(x + xr * ldx + up_off + j * 16);
         u0 = __ldg(up);
         u1 = __ldg(up + 1);
       }
@@ -566,9 +583,11 @@ namespace {
 constexpr bool kPosQuant = true;
 constexpr int kPosQuantBlocksPerSm = 16;
 
+// src_rows != nullptr: row r of the input is row src_rows[r] of x [tokens, k] (gather fused in).
 nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t t, int64_t k, int64_t ldx,
                             const int64_t *row_offsets, int num_experts, const float *gs, uint8_t *q, uint8_t *sf,
-                            size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream) {
+                            size_t sf_bytes, uint32_t flags, nvfp4_stream_t stream,
+                            const int32_t *src_rows = nullptr, int64_t tokens = 0) {
   clear_error();
   if (t < 0 || k <= 0 || k >= (1LL << 31)) return fail(NVFP4_ERR_INVALID_ARG, "%s: t=%lld k=%lld", name, (long long)t, (long long)k);
   if (k % 16) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: k=%lld is not a multiple of 16", name, (long long)k);
@@ -584,6 +603,7 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
   if (sf_bytes < need) return fail(NVFP4_ERR_INVALID_ARG, "%s: sf_bytes=%zu < %zu", name, sf_bytes, need);
   if (t == 0) return NVFP4_OK;
   if (!x || !row_offsets || !gs || !q || !sf) return fail(NVFP4_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (src_rows && !aligned(src_rows, 4)) return fail(NVFP4_ERR_MISALIGNED, "%s: src_rows needs 4-B alignment", name);
   if (!aligned(x, 16) || !aligned(q, 8) || !aligned(sf, 16) || !aligned(row_offsets, 8) || !aligned(gs, 4))
     return fail(NVFP4_ERR_MISALIGNED, "%s: x 16-B, q 8-B, sf 16-B, row_offsets 8-B, gs 4-B alignment", name);
   DeviceInfo dev;
@@ -591,14 +611,17 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
   if (st != NVFP4_OK) return st;
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
   const int64_t scale_rows = round_up(t, 128) + 128LL * num_experts;  // bound of sum_e round_up(M_e, 128)
+  if (src_rows && scale_rows * cp >= (1LL << 31))
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "%s: (rows + 128 experts) * k/16 >= 2^31 positions", name);
   if (kPosQuant && scale_rows * cp < (1LL << 31)) {
-    auto kern = silu ? expert_quant_pos_kernel<true> : expert_quant_pos_kernel<false>;
+    auto kern = src_rows ? expert_quant_pos_kernel<false, true>
+                         : (silu ? expert_quant_pos_kernel<true, false> : expert_quant_pos_kernel<false, false>);
     const int64_t blocks = ceil_div(scale_rows * cp, 256);
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * kPosQuantBlocksPerSm;
     cudaError_t e = launch(kern, dim3(static_cast<int>(blocks < cap ? blocks : cap)), dim3(256), 0,
                            (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x),
                            t, static_cast<int>(k / 16), ldx, silu ? k : static_cast<int64_t>(0), row_offsets, num_experts,
-                           gs, q, sf, cap_rows, static_cast<int>(cp));
+                           gs, q, sf, cap_rows, static_cast<int>(cp), src_rows, tokens, dev.status);
     return check_launch(e, name);
   }
   auto kern = silu ? expert_quant_kernel<true> : expert_quant_kernel<false>;
@@ -616,6 +639,18 @@ extern "C" nvfp4_status_t nvfp4_quantize_experts(const void *x, int64_t t, int64
                                                  nvfp4_stream_t stream) {
   return expert_quant("nvfp4_quantize_experts", false, x, t, k, ldx, row_offsets, num_experts, gs, q, sf, sf_bytes,
                       flags, stream);
+}
+
+extern "C" nvfp4_status_t nvfp4_gather_quantize_experts(const void *x, int64_t num_tokens, int64_t k, int64_t ldx,
+                                                        const int32_t *src_rows, int64_t rows,
+                                                        const int64_t *row_offsets, int num_experts, const float *gs,
+                                                        uint8_t *q, uint8_t *sf, size_t sf_bytes, uint32_t flags,
+                                                        nvfp4_stream_t stream) {
+  clear_error();
+  if (num_tokens < 0) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gather_quantize_experts: num_tokens=%lld", (long long)num_tokens);
+  if (rows > 0 && !src_rows) return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_gather_quantize_experts: null pointer");
+  return expert_quant("nvfp4_gather_quantize_experts", false, x, rows, k, ldx, row_offsets, num_experts, gs, q, sf,
+                      sf_bytes, flags, stream, src_rows, num_tokens);
 }
 
 extern "C" nvfp4_status_t nvfp4_silu_mul_quantize_experts(const void *x, int64_t t, int64_t inter, int64_t ldx,

@@ -213,6 +213,14 @@ def test_moe_steps_reject_bad_arguments_without_a_device(lib):
         assert f(_c(X), 40, k, ldx, _c(R), 4, _c(G), _c(Q + 4), _c(S), sfb, 0, None) == 2  # q 8-B
         assert f(_c(X), 40, k, ldx, None, 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 1
         assert f(None, 0, k, ldx, None, 4, None, None, None, sfb, 0, None) == 0           # no rows
+    gq = L.nvfp4_gather_quantize_experts                                               # x: 16 tokens
+    assert gq(_c(X), -1, 256, 256, _c(P), 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 1   # tokens < 0
+    assert gq(_c(X), 16, 256, 256, None, 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 1    # no src_rows
+    assert gq(_c(X), 16, 256, 256, _c(P + 2), 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 2  # src 4-B
+    assert gq(_c(X), 16, 250, 256, _c(P), 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 3   # k % 16
+    assert gq(_c(X), 16, 256, 248, _c(P), 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb, 0, None) == 2   # ldx < k
+    assert gq(_c(X), 16, 256, 256, _c(P), 40, _c(R), 4, _c(G), _c(Q), _c(S), sfb - 1, 0, None) == 1  # sf small
+    assert gq(None, 0, 256, 256, None, 0, None, 4, None, None, None, sfb, 0, None) == 0          # no rows
 
 
 def test_noalloc_gemm_refuses_what_nvfp4_gemm_refuses_without_a_device(lib):

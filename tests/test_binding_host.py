@@ -127,6 +127,9 @@ def test_moe_steps(nv):
     gs = f32(E)
     q1, s1 = nv.nvfp4_quantize_experts(xg, ro, gs)
     nv.nvfp4_quantize_experts(xg, ro, gs, q=u8(R, H // 2), sf=u8(nv.expert_sf_bytes(R, E, H)))
+    qg, sg = nv.nvfp4_gather_quantize_experts(bf(T, H), src, ro, gs)
+    assert qg.shape == (R, H // 2) and sg.numel() == nv.expert_sf_bytes(R, E, H)
+    nv.nvfp4_gather_quantize_experts(bf(T, H), src, ro, gs, q=u8(R, H // 2), sf=u8(nv.expert_sf_bytes(R, E, H)))
     qw, sfw = u8(E, 2 * I, H // 2), u8(E, nv.sf_bytes(2 * I, H, 16))
     h1 = nv.nvfp4_grouped_gemm(q1, s1, ro, qw, sfw, f32(E))
     q2, s2 = nv.nvfp4_silu_mul_quantize_experts(h1, ro, gs)
@@ -140,6 +143,10 @@ def test_moe_steps(nv):
         nv.moe_combine(y, pos, f32(T, topk + 1))
     with pytest.raises(ValueError, match="gs has"):
         nv.nvfp4_quantize_experts(xg, ro, f32(E - 1))
+    with pytest.raises(ValueError, match="q has"):
+        nv.nvfp4_gather_quantize_experts(bf(T, H), src, ro, gs, q=u8(R - 1, H // 2))
+    with pytest.raises(TypeError, match="src_rows"):
+        nv.nvfp4_gather_quantize_experts(bf(T, H), src.long(), ro, gs)
     with pytest.raises(ValueError, match="pos has"):
         nv.moe_sort_by_expert(ids, E, out=(ro, src, torch.zeros(R - 1, dtype=torch.int32)))
     assert nv.calls.count("moe_combine") == 1

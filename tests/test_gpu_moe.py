@@ -1,5 +1,5 @@
 """GPU parity of the NVFP4 MoE steps against oracle/moe.py: the expert sort, gather and combine
-bit-exact, the per-expert quantisers (plain and SiLU-fused) bit-exact, the NVFP4 grouped GEMM
+bit-exact, the per-expert quantisers (plain, gather-fused and SiLU-fused) bit-exact, the NVFP4 grouped GEMM
 within |D - R| <= ulp_bf16(|R|) + 1e-5 * sum_k |alpha a b|; and the whole layer chained, each
 step checked on the GPU's own input to it."""
 import numpy as np
@@ -85,6 +85,51 @@ def test_quantize_experts_bit_exact(nv, counts, k):
     q, sf = nv.nvfp4_quantize_experts(x.cuda(), torch.from_numpy(ro).cuda(), torch.from_numpy(gs).cuda())
     torch.cuda.synchronize()
     oq, osf = moe.nvfp4_quantize_experts(x, ro, gs)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(sf.cpu().numpy()[:osf.size], osf)
+
+
+@pytest.mark.parametrize("T,E,topk,k,pad", [(1, 1, 1, 64, 0), (7, 4, 2, 96, 8), (300, 16, 8, 2048, 0),
+                                             (1000, 128, 8, 768, 16)])
+def test_gather_quantize_experts_bit_exact(nv, T, E, topk, k, pad):
+    """The fused gather + quantise against the oracle's quantiser on the oracle-gathered rows,
+    and bit for bit against the two separate device steps; x may have a row stride above k."""
+    ids, _ = _route(T, E, topk, 7 * T + k)
+    o_ro, o_src, _ = moe.sort_by_expert(ids.numpy(), E)
+    xf = synth.activation(T + k + 1, T, k + pad, outliers=False)
+    x = xf[:, :k]
+    gs = (np.random.default_rng(k + 1).uniform(100, 3000, E)).astype(F32)
+    x_d, ro_d, gs_d = xf.cuda()[:, :k], torch.from_numpy(o_ro).cuda(), torch.from_numpy(gs).cuda()
+    src_d = torch.from_numpy(o_src.astype(np.int32)).cuda()
+    q, sf = nv.nvfp4_gather_quantize_experts(x_d, src_d, ro_d, gs_d)
+    torch.cuda.synchronize()
+    nv.check_status()
+    oq, osf = moe.nvfp4_quantize_experts(x[torch.from_numpy(o_src)], o_ro, gs)
+    assert np.array_equal(q.cpu().numpy(), oq)
+    assert np.array_equal(sf.cpu().numpy()[:osf.size], osf)
+    q2, sf2 = nv.nvfp4_quantize_experts(nv.moe_gather_rows(x_d, src_d), ro_d, gs_d)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(sf[:osf.size], sf2[:osf.size])
+
+
+def test_gather_quantize_flags_a_bad_source_row(nv):
+    """A source index outside [0, tokens) quantises zeros for that row and is reported."""
+    T, E, topk, k = 40, 4, 2, 128
+    ids, _ = _route(T, E, topk, 3)
+    o_ro, o_src, _ = moe.sort_by_expert(ids.numpy(), E)
+    bad = o_src.astype(np.int32)
+    bad[5] = T
+    bad[17] = -1
+    x = synth.activation(9, T, k, outliers=False)
+    gs = np.full(E, 700.0, F32)
+    q, sf = nv.nvfp4_gather_quantize_experts(x.cuda(), torch.from_numpy(bad).cuda(), torch.from_numpy(o_ro).cuda(),
+                                             torch.from_numpy(gs).cuda())
+    with pytest.raises(nv.NVFP4Error, match="out of range"):
+        nv.check_status()
+    xg = x[torch.from_numpy(o_src)].clone()
+    xg[5] = 0
+    xg[17] = 0
+    oq, osf = moe.nvfp4_quantize_experts(xg, o_ro, gs)
     assert np.array_equal(q.cpu().numpy(), oq)
     assert np.array_equal(sf.cpu().numpy()[:osf.size], osf)
 
