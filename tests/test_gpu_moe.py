@@ -75,7 +75,12 @@ def _counts_to_offsets(counts):
 
 
 @pytest.mark.parametrize("counts,k", [([5], 64), ([0, 3, 130, 0, 1, 64], 96), ([256] * 4, 2048),
-                                      (list(np.random.default_rng(0).integers(0, 300, 128)), 768)])
+                                      (list(np.random.default_rng(0).integers(0, 300, 128)), 768),
+                                      # 1024 experts, many empty: the expert table at its widest
+                                      (list(np.random.default_rng(2).integers(0, 3, 1024) * 7), 64),
+                                      # 4376 128-row scale blocks: more than the table holds, so
+                                      # each position searches the scale-row prefix instead
+                                      ([300000, 0, 260000], 64)])
 def test_quantize_experts_bit_exact(nv, counts, k):
     ro = _counts_to_offsets(counts)
     T = int(ro[-1])
