@@ -277,7 +277,7 @@ size_t moe_sort_workspace_size(int64_t num_tokens, int num_experts);
  *   workspace    DEVICE, 4-B aligned, workspace_bytes >= moe_sort_workspace_size(); no
  *                initialisation needed (every byte used is written first)
  * Inside an expert, rows keep (token, slot) row-major order.  1 <= topk <= 32,
- * 1 <= num_experts <= 1024.  Two kernels over ceil(num_tokens/32) CTAs (at most 1024). */
+ * 1 <= num_experts <= 1024, num_tokens * topk <= 2^31 - 512.  Two kernels over ceil(num_tokens/32) CTAs (at most 1024). */
 nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t num_tokens, int topk, int num_experts,
                                   int64_t *row_offsets, int32_t *src_rows, int32_t *pos, int32_t *workspace,
                                   size_t workspace_bytes, uint32_t flags, nvfp4_stream_t stream);

@@ -57,6 +57,9 @@ inline bool aligned(const void *p, uintptr_t a) {
 }
 inline int64_t round_up(int64_t x, int64_t y) { return (x + y - 1) / y * y; }
 inline int64_t ceil_div(int64_t x, int64_t y) { return (x + y - 1) / y; }
+// A grid-stride loop over `total` positions may count in 32-bit signed integers only when the
+// last position plus one stride still fits: then no step wraps.
+inline bool fits_i32_loop(int64_t total, int64_t grid_threads) { return total + grid_threads < (1LL << 31); }
 
 // cudaLaunchKernelEx with optional programmatic-dependent-launch and cluster attributes.
 template <typename... KArgs, typename... Args>

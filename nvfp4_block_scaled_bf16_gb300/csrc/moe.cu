@@ -544,8 +544,9 @@ extern "C" nvfp4_status_t moe_sort_by_expert(const int32_t *topk_ids, int64_t nu
                                              size_t workspace_bytes, uint32_t flags, nvfp4_stream_t stream) {
   clear_error();
   if (num_tokens < 0 || topk < 1 || topk > 32 || num_experts < 1 || num_experts > kMaxExpertsMoe ||
-      num_tokens * topk >= (1LL << 31))
-    return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: tokens=%lld topk=%d experts=%d (topk 1..32, experts 1..%d)",
+      num_tokens * topk > (1LL << 31) - 512)  // the kernels' 32-bit slot loops step past the end by < 512
+    return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: tokens=%lld topk=%d experts=%d (topk 1..32, experts 1..%d, "
+                "tokens * topk <= 2^31 - 512)",
                 (long long)num_tokens, topk, num_experts, kMaxExpertsMoe);
   if (flags & ~(uint32_t)NVFP4_FLAG_PDL) return fail(NVFP4_ERR_INVALID_ARG, "moe_sort_by_expert: unknown flags 0x%x", flags);
   const size_t need = moe_sort_workspace_size(num_tokens, num_experts);
@@ -589,8 +590,9 @@ extern "C" nvfp4_status_t moe_gather_rows(const void *x, int64_t num_tokens, int
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   const int64_t pieces = h / 8;
-  auto kern = rows * pieces < (1LL << 31) ? moe_gather_kernel<int> : moe_gather_kernel<int64_t>;
-  cudaError_t e = launch(kern, dim3(moe_grid(rows * pieces, dev.sm_count, kMoveBlocksPerSm)), dim3(256), 0,
+  const int grid = moe_grid(rows * pieces, dev.sm_count, kMoveBlocksPerSm);
+  auto kern = fits_i32_loop(rows * pieces, grid * 256LL) ? moe_gather_kernel<int> : moe_gather_kernel<int64_t>;
+  cudaError_t e = launch(kern, dim3(grid), dim3(256), 0,
                          (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(x),
                          ldx / 8, num_tokens, src_rows, rows, pieces, static_cast<uint4 *>(out), dev.status);
   return check_launch(e, "moe_gather_rows");
@@ -612,9 +614,9 @@ extern "C" nvfp4_status_t moe_combine(const void *y, int64_t rows, const int32_t
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
   const int64_t pieces = h / 8;
-  const bool narrow = num_tokens * pieces < (1LL << 31);
-  auto kern = narrow ? moe_combine_kernel<int> : moe_combine_kernel<int64_t>;
-  cudaError_t e = launch(kern, dim3(moe_grid(num_tokens * pieces, dev.sm_count, kMoveBlocksPerSm)), dim3(256), 0,
+  const int grid = moe_grid(num_tokens * pieces, dev.sm_count, kMoveBlocksPerSm);
+  auto kern = fits_i32_loop(num_tokens * pieces, grid * 256LL) ? moe_combine_kernel<int> : moe_combine_kernel<int64_t>;
+  cudaError_t e = launch(kern, dim3(grid), dim3(256), 0,
                          (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const uint4 *>(y), rows,
                          pos, weights, num_tokens, topk, pieces, static_cast<uint4 *>(out), dev.status);
   return check_launch(e, "moe_combine");

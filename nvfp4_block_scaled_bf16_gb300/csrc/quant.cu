@@ -201,7 +201,7 @@ extern "C" nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, in
   const int64_t cp = round_up(k / 16, 4);
   const int64_t total = round_up(m, 128) * cp;
   const int grid = quant_grid(total, dev.sm_count);
-  const bool narrow = total < (1LL << 31);
+  const bool narrow = fits_i32_loop(total, static_cast<int64_t>(grid) * 256);
   auto kern = (flags & NVFP4_FLAG_SF_SM103) ? (narrow ? nvfp4_quant_kernel<true, int> : nvfp4_quant_kernel<true, int64_t>)
                                             : (narrow ? nvfp4_quant_kernel<false, int> : nvfp4_quant_kernel<false, int64_t>);
   cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
@@ -236,8 +236,8 @@ extern "C" nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, in
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
   const int64_t total = (row_offsets ? round_up(t, 128) + 128LL * num_experts : round_up(t, 128)) * cp;
   const int grid = quant_grid(total, dev.sm_count);
-  // (the kernel's positions cover at most `total`: 32-bit when that fits)
-  auto kern = total < (1LL << 31) ? mxfp4_quant_kernel<int> : mxfp4_quant_kernel<int64_t>;
+  // (the kernel's positions cover at most `total`: 32-bit when that plus one grid stride fits)
+  auto kern = fits_i32_loop(total, static_cast<int64_t>(grid) * 256) ? mxfp4_quant_kernel<int> : mxfp4_quant_kernel<int64_t>;
   cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, t, k / 32,
                          ldx, row_offsets, row_offsets ? num_experts : 1, q, sf, cap_rows, cp);

@@ -187,6 +187,7 @@ def test_moe_steps_reject_bad_arguments_without_a_device(lib):
     sort = L.moe_sort_by_expert
     assert sort(_c(I), 16, 33, 4, _c(R), _c(P), _c(P), _c(W), ws, 0, None) == 1      # topk > 32
     assert sort(_c(I), 16, 2, 1025, _c(R), _c(P), _c(P), _c(W), 1 << 30, 0, None) == 1  # experts > 1024
+    assert sort(_c(I), (1 << 31) - 511, 1, 4, _c(R), _c(P), _c(P), _c(W), 1 << 30, 0, None) == 1  # slots > 2^31-512
     assert sort(_c(I), 16, 2, 4, _c(R), _c(P), _c(P), _c(W), ws - 1, 0, None) == 1   # workspace too small
     assert "workspace" in lib.last_error()
     assert sort(_c(I), 16, 2, 4, _c(R), _c(P), _c(P), _c(W), ws, 1 << 2, None) == 1  # flags
