@@ -178,6 +178,28 @@ nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_
   return NVFP4_OK;
 }
 
+int resident_blocks(const void *fn, int threads) {
+  struct Entry {
+    const void *fn;
+    int threads, blocks;
+  };
+  static Entry cache[64];
+  static int n = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < n; ++i)
+      if (cache[i].fn == fn && cache[i].threads == threads) return cache[i].blocks;
+  }
+  int blocks = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, threads, 0) != cudaSuccess || blocks < 1) {
+    cudaGetLastError();  // consume the error so later calls do not see it
+    return 1;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (n < 64) cache[n++] = Entry{fn, threads, blocks};
+  return blocks;
+}
+
 nvfp4_status_t allow_smem(const void *fn, int bytes, int device) {
   const unsigned long long ctx = current_context_id();
   if (ctx != 0) {

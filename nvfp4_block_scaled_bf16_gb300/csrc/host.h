@@ -52,6 +52,11 @@ nvfp4_status_t encode_tmap_stages_u8(CUtensorMap *map, const void *base, uint64_
 // Raises the dynamic shared-memory limit of `fn` on the current device (once per device).
 nvfp4_status_t allow_smem(const void *fn, int bytes, int device);
 
+// Blocks of `threads` threads (no dynamic shared memory) of kernel `fn` resident on one SM, by
+// the occupancy calculator; cached per kernel, since it depends only on the compiled code.
+// 1 if the query fails.
+int resident_blocks(const void *fn, int threads);
+
 inline bool aligned(const void *p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

@@ -7,8 +7,6 @@
 // nvfp4.h.  All of these are bandwidth-bound CUDA-core kernels.
 #include <cuda_bf16.h>
 
-#include <atomic>
-
 #include "host.h"
 #include "ptx.cuh"
 
@@ -627,22 +625,6 @@ namespace {
 // scale row).
 constexpr bool kPosQuant = true;
 
-// 256-thread blocks of a position-quantiser variant resident on one SM.  The position form
-// launches exactly that many per SM: every block pays the prologue (offsets, prefix, expert table)
-// once and walks its share of positions, which measured faster than 16 or 2x-resident blocks
-// per SM (plain 32.8 -> 30.7 us, gathered 41.0 -> 39.7, SiLU 47.1 -> 45.1 at 128 experts,
-// 32768 rows).  Cached per variant: it depends only on the compiled kernel.
-int pos_quant_blocks_per_sm(const void *kern, int variant) {
-  static std::atomic<int> cache[3];
-  int occ = cache[variant].load(std::memory_order_relaxed);
-  if (occ > 0) return occ;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 256, 0) != cudaSuccess || occ < 1) {
-    cudaGetLastError();
-    occ = 4;
-  }
-  cache[variant].store(occ, std::memory_order_relaxed);
-  return occ;
-}
 
 // src_rows != nullptr: row r of the input is row src_rows[r] of x [tokens, k] (gather fused in).
 nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t t, int64_t k, int64_t ldx,
@@ -677,10 +659,12 @@ nvfp4_status_t expert_quant(const char *name, bool silu, const void *x, int64_t 
   if (kPosQuant && scale_rows * cp < (1LL << 31)) {
     auto kern = src_rows ? expert_quant_pos_kernel<false, true>
                          : (silu ? expert_quant_pos_kernel<true, false> : expert_quant_pos_kernel<false, false>);
-    const int variant = src_rows ? 2 : (silu ? 1 : 0);
+    // Exactly the resident blocks per SM: every block pays the prologue (offsets, prefix, expert
+    // table) once and walks its share of positions, which measured faster than 16 or twice the
+    // resident blocks per SM (plain 32.8 -> 30.7 us, gathered 41.0 -> 39.7, SiLU 47.1 -> 45.1 at
+    // 128 experts, 32768 rows).
     const int64_t blocks = ceil_div(scale_rows * cp, 256);
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) *
-                        pos_quant_blocks_per_sm(reinterpret_cast<const void *>(kern), variant);
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * resident_blocks(reinterpret_cast<const void *>(kern), 256);
     cudaError_t e = launch(kern, dim3(static_cast<int>(blocks < cap ? blocks : cap)), dim3(256), 0,
                            (cudaStream_t)stream, (flags & NVFP4_FLAG_PDL) != 0, 1, static_cast<const __nv_bfloat16 *>(x),
                            t, static_cast<int>(k / 16), ldx, silu ? k : static_cast<int64_t>(0), row_offsets, num_experts,

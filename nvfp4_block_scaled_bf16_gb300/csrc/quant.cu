@@ -64,9 +64,15 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *_
   pdl_wait();
   const float gs = __ldg(gs_ptr);
   const I stride = static_cast<I>(gridDim.x) * blockDim.x;
-  for (I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int64_t r = idx / cp;
-    const int64_t j = idx - static_cast<I>(r) * cp;
+  I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // (row, scale column) of idx, stepped by the grid stride instead of a division per position
+  I r = idx / cp, j = idx - (idx / cp) * cp;
+  const I dr = stride / cp, dj = stride - dr * cp;
+  for (; idx < total; idx += stride, r += dr, j += dj) {
+    if (j >= cp) {
+      j -= cp;
+      ++r;
+    }
     uint32_t code = 0;
     if (r < m && j < kb) {
       const uint4 *src = reinterpret_cast<const uint4 *>(x + r * ldx + j * 16);
@@ -80,6 +86,9 @@ __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *_
 }
 
 constexpr int kMaxExperts = 1024;
+// 128-row scale blocks whose owning expert the grouped quantiser tabulates in shared memory
+// (8 KB; 512K scale rows); beyond that it searches the scale-row prefix per position.
+constexpr int kExpertBlockTable = 4096;
 
 // Scale rows of the (optionally expert-grouped) MXFP4 layout: expert e owns scale rows
 // sfr[e] .. sfr[e+1]-1, sfr[e+1] - sfr[e] = round_up(M_e, 128).
@@ -92,6 +101,7 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
                                                           int64_t cap_rows, int64_t cp) {
   __shared__ int64_t s_ro[kMaxExperts + 1];
   __shared__ int64_t s_sfr[kMaxExperts + 1];
+  __shared__ uint16_t s_blk[kExpertBlockTable];
   // Let the next kernel launch at once (it waits for this grid's completion before it reads
   // our outputs), then wait for our own predecessor before reading x.
   pdl_trigger();
@@ -129,18 +139,46 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
     }
   }
   __syncthreads();
+  // Every expert owns whole 128-row blocks of scale rows: with at most kExpertBlockTable of them
+  // a table filled by one search per entry gives a position's expert in one lookup.
+  const int64_t nblk = s_sfr[experts] >> 7;
+  const bool table = experts > 1 && nblk >= 0 && nblk <= kExpertBlockTable;
+  if (table) {
+    for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+      const int64_t row0 = static_cast<int64_t>(b) << 7;
+      int lo = 0, hi = experts - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_sfr[mid] <= row0) lo = mid;
+        else hi = mid - 1;
+      }
+      s_blk[b] = static_cast<uint16_t>(lo);
+    }
+    __syncthreads();
+  }
   const int64_t rows = s_sfr[experts] < cap_rows ? s_sfr[experts] : cap_rows;
-  const I total = static_cast<I>(rows * cp), cpi = static_cast<I>(cp);
+  const I total = static_cast<I>(rows > 0 ? rows * cp : 0), cpi = static_cast<I>(cp);
   const I stride = static_cast<I>(gridDim.x) * blockDim.x;
-  for (I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int64_t s = idx / cpi;
-    const int64_t j = idx - static_cast<I>(s) * cpi;
-    // expert owning scale row s: the largest e with s_sfr[e] <= s
-    int lo = 0, hi = experts - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_sfr[mid] <= s) lo = mid;
-      else hi = mid - 1;
+  I idx = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // (scale row, scale column) of idx, stepped by the grid stride instead of a division each
+  I s = idx / cpi, j = idx - (idx / cpi) * cpi;
+  const I ds = stride / cpi, dj = stride - ds * cpi;
+  for (; idx < total; idx += stride, s += ds, j += dj) {
+    if (j >= cpi) {
+      j -= cpi;
+      ++s;
+    }
+    int lo;  // expert owning scale row s: the largest e with s_sfr[e] <= s
+    if (table) {
+      lo = s_blk[s >> 7];  // s < rows <= 128 * nblk; every entry holds an expert in range
+    } else {
+      lo = 0;
+      int hi = experts - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_sfr[mid] <= s) lo = mid;
+        else hi = mid - 1;
+      }
     }
     const int64_t local = s - s_sfr[lo];
     const int64_t r = s_ro[lo] + local;
@@ -171,9 +209,11 @@ __global__ void __launch_bounds__(256) mxfp4_quant_kernel(const __nv_bfloat16 *_
   }
 }
 
-int quant_grid(int64_t total_threads, int sm_count) {
+// At most the blocks of `kern` resident on every SM at once: a block walks its share of the
+// positions, and its prologue runs once.
+int quant_grid(int64_t total_threads, int sm_count, const void *kern) {
   const int64_t blocks = ceil_div(total_threads, 256);
-  const int64_t cap = static_cast<int64_t>(sm_count) * 16;
+  const int64_t cap = static_cast<int64_t>(sm_count) * resident_blocks(kern, 256);
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
@@ -200,10 +240,13 @@ extern "C" nvfp4_status_t nvfp4_quantize(const void *x, int64_t m, int64_t k, in
   if (st != NVFP4_OK) return st;
   const int64_t cp = round_up(k / 16, 4);
   const int64_t total = round_up(m, 128) * cp;
-  const int grid = quant_grid(total, dev.sm_count);
-  const bool narrow = fits_i32_loop(total, static_cast<int64_t>(grid) * 256);
-  auto kern = (flags & NVFP4_FLAG_SF_SM103) ? (narrow ? nvfp4_quant_kernel<true, int> : nvfp4_quant_kernel<true, int64_t>)
-                                            : (narrow ? nvfp4_quant_kernel<false, int> : nvfp4_quant_kernel<false, int64_t>);
+  const bool sm103 = (flags & NVFP4_FLAG_SF_SM103) != 0;
+  auto kern = sm103 ? nvfp4_quant_kernel<true, int> : nvfp4_quant_kernel<false, int>;
+  int grid = quant_grid(total, dev.sm_count, reinterpret_cast<const void *>(kern));
+  if (!fits_i32_loop(total, static_cast<int64_t>(grid) * 256)) {
+    kern = sm103 ? nvfp4_quant_kernel<true, int64_t> : nvfp4_quant_kernel<false, int64_t>;
+    grid = quant_grid(total, dev.sm_count, reinterpret_cast<const void *>(kern));
+  }
   cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, m, k / 16,
                          ldx, gs, q, sf, total, cp);
@@ -235,9 +278,13 @@ extern "C" nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, in
   const int64_t cp = round_up(k / 32, 4);
   const int64_t cap_rows = static_cast<int64_t>(sf_bytes) / cp / 128 * 128;
   const int64_t total = (row_offsets ? round_up(t, 128) + 128LL * num_experts : round_up(t, 128)) * cp;
-  const int grid = quant_grid(total, dev.sm_count);
   // (the kernel's positions cover at most `total`: 32-bit when that plus one grid stride fits)
-  auto kern = fits_i32_loop(total, static_cast<int64_t>(grid) * 256) ? mxfp4_quant_kernel<int> : mxfp4_quant_kernel<int64_t>;
+  auto kern = mxfp4_quant_kernel<int>;
+  int grid = quant_grid(total, dev.sm_count, reinterpret_cast<const void *>(kern));
+  if (!fits_i32_loop(total, static_cast<int64_t>(grid) * 256)) {
+    kern = mxfp4_quant_kernel<int64_t>;
+    grid = quant_grid(total, dev.sm_count, reinterpret_cast<const void *>(kern));
+  }
   cudaError_t e = launch(kern, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
                          (flags & NVFP4_FLAG_PDL) != 0, 1, (const __nv_bfloat16 *)x, t, k / 32,
                          ldx, row_offsets, row_offsets ? num_experts : 1, q, sf, cap_rows, cp);
