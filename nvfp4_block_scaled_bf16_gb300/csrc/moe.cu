@@ -209,6 +209,10 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const uint4 *__restric
 // Both run on two values at once with Blackwell's packed fp32 instructions (mul/add/sub
 // .rn.f32x2 round each lane to nearest even exactly as the scalar forms, so each lane's result
 // is that of the scalar steps); the range tests are per-lane selects after the polynomial.
+// rint: adding 1.5 * 2^23 rounds to an integer (nearest even) for |x| < 2^22 and leaves it in
+// the low mantissa bits; subtracting it again gives rint(x) exactly.  Larger |x| only occur for
+// t outside [-87, 88], whose results the selects replace.  This keeps the float<->int
+// conversions, a low-rate pipe, off the path (SiLU form 45.0 -> 43.3 us, bit-identical).
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
@@ -234,10 +238,12 @@ __device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
 }
 __device__ __forceinline__ uint64_t exp_cw2(float t0, float t1) {
   const uint64_t t = pk2(t0, t1);
-  float m0, m1;
-  upk2(mul2(t, pk2(1.44269502162933349609375f, 1.44269502162933349609375f)), m0, m1);
-  const int i0 = __float2int_rn(m0), i1 = __float2int_rn(m1);
-  const uint64_t n = pk2(__int2float_rn(i0), __int2float_rn(i1));
+  const uint64_t m = mul2(t, pk2(1.44269502162933349609375f, 1.44269502162933349609375f));
+  const uint64_t sh = add2(m, pk2(12582912.0f, 12582912.0f));  // 1.5 * 2^23
+  const uint64_t n = sub2(sh, pk2(12582912.0f, 12582912.0f));   // rint(m), exact
+  float sh0, sh1;
+  upk2(sh, sh0, sh1);
+  const int i0 = __float_as_int(sh0) - 0x4B400000, i1 = __float_as_int(sh1) - 0x4B400000;  // rint(m) as int
   const uint64_t r = sub2(sub2(t, mul2(n, pk2(0.693145751953125f, 0.693145751953125f))),
                           mul2(n, pk2(1.428606765330187045037746429443359375e-06f, 1.428606765330187045037746429443359375e-06f)));
   const float c[7] = {1.388888922519981861114501953125e-03f, 8.333333767950534820556640625e-03f,
@@ -258,8 +264,9 @@ __device__ __forceinline__ void silu_mul_bf16x2(float &g0, float &g1, float u0, 
   const uint64_t sig = pk2(__fdiv_rn(1.0f, d0), __fdiv_rn(1.0f, d1));
   float h0, h1;
   upk2(mul2(mul2(pk2(g0, g1), sig), pk2(u0, u1)), h0, h1);
-  g0 = __bfloat162float(__float2bfloat16_rn(h0));
-  g1 = __bfloat162float(__float2bfloat16_rn(h1));
+  const uint32_t hb = pack_bf16x2(h0, h1);
+  g0 = __uint_as_float(hb << 16);
+  g1 = __uint_as_float(hb & 0xFFFF0000u);
 }
 
 __device__ __forceinline__ void bf16x8_to_f32_moe(const uint4 &v, float *f) {
