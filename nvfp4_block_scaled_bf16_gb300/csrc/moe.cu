@@ -59,31 +59,61 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) moe_place_kernel(const int32
   pdl_trigger();
   pdl_wait();
   const int G = gridDim.x, g = blockIdx.x;
-  // expert totals and the part of each expert that earlier CTAs own
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int before = 0, total = 0;
-    for (int h = 0; h < G; ++h) {
-      const int v = hist[static_cast<int64_t>(h) * E + e];
-      before += h < g ? v : 0;
-      total += v;
-    }
-    scan[e] = total;
-    base[e] = before;
+    scan[e] = 0;
+    base[e] = 0;
   }
   for (int i = threadIdx.x; i < kPlaceWarps * E; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {  // exclusive prefix of the totals (E <= 1024 adds)
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      const int v = scan[e];
-      scan[e] = acc;
-      acc += v;
-      if (g == 0) row_offsets[e] = acc - v;
+  // Expert totals and the part of each expert that earlier CTAs own.  P threads share an expert's
+  // column of the count table (strided over the CTAs), each with 8 loads in flight, and add
+  // their integer partials into shared memory: a CTA's walk of the table is ~G/(8P) load
+  // latencies instead of G.
+  const int P = E < static_cast<int>(blockDim.x) ? static_cast<int>(blockDim.x) / E : 1;
+  for (int i = threadIdx.x; i < E * P; i += blockDim.x) {
+    const int e = i % E, p = i / E;
+    int before = 0, total = 0;
+    int h = p;
+    for (; h + 7 * P < G; h += 8 * P) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = hist[static_cast<int64_t>(h + u * P) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        total += v[u];
+        before += h + u * P < g ? v[u] : 0;
+      }
     }
-    if (g == 0) row_offsets[E] = acc;
+    for (; h < G; h += P) {
+      const int v = hist[static_cast<int64_t>(h) * E + e];
+      total += v;
+      before += h < g ? v : 0;
+    }
+    atomicAdd(&scan[e], total);
+    atomicAdd(&base[e], before);
   }
   __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (warp == 0) {  // exclusive prefix of the totals: a warp scan, 32 experts at a time
+    int carry = 0;
+    for (int b0 = 0; b0 < E; b0 += 32) {
+      const int e = b0 + lane;
+      const int v = e < E ? scan[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (e < E) {
+        scan[e] = carry + incl - v;
+        if (g == 0) row_offsets[e] = carry + incl - v;
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (g == 0 && lane == 0) row_offsets[E] = carry;
+  }
+  __syncthreads();
   const int t0 = g * tpc, t1 = min(T, t0 + tpc);
   const int tpw = (t1 - t0 + kPlaceWarps - 1) / kPlaceWarps;
   const int w0 = min(t1, t0 + warp * tpw), w1 = min(t1, w0 + tpw);
