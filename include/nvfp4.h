@@ -142,7 +142,10 @@ nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, int64_t ldx,
 
 /* The tile configuration nvfp4_gemm picks for a shape (M-based selector, [vLLM-SM103]
  * nvfp4_scaled_mm_kernels.cu "SM103 Dispatch"; narrow tiles for small M, [FI-4865]
- * "Reviewer Notes").  Host only. */
+ * "Reviewer Notes").  Up to 256 tokens the weight fills the MMA's 128-row slot and K is split
+ * inside clusters, except where 256 x 256 CTA-pair tiles fill a quarter of the pairs, or where K
+ * is at most 2048 (17 or more tokens, 4096 <= N <= 16384): there whole 128 x 128 tiles run.
+ * Host only. */
 typedef struct {
   int swap_ab;   /* 1: the weight B fills the 128-row MMA slot and tokens the N slot */
   int tile_m;    /* rows of the MMA tile (128) */
@@ -198,7 +201,9 @@ nvfp4_status_t nvfp4_gemm(const uint8_t *a, const uint8_t *sfa, const uint8_t *b
  *   b, sfb, alpha, d, workspace, flags, stream: as nvfp4_gemm (NVFP4_FLAG_SF_SM103: sfb is in
  *          the SM103 layout); these plans split K inside clusters and need no workspace.
  *   1 <= m <= 256 (the weight-streaming plans, where each CTA quantises the token rows it
- *   needs); larger m: NVFP4_ERR_UNSUPPORTED_SHAPE, nothing launched (quantise separately).
+ *   needs; this call takes one for every such m, also where nvfp4_gemm_plan reports another
+ *   kind for nvfp4_gemm); larger m: NVFP4_ERR_UNSUPPORTED_SHAPE, nothing launched (quantise
+ *   separately).
  *   Every CTA that shares a token tile quantises it again (once per 128 weight rows), so the
  *   fused call is faster than the PDL-chained pair only for a few tokens (measured on GB300,
  *   N=4096, K=7168, cold weights: M=1 3 % faster, M=4 even, M >= 16 slower).

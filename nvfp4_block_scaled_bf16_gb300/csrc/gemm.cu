@@ -56,7 +56,9 @@ int max_contributors(int64_t sk_tiles, int k_tiles, int ctas) {
   return static_cast<int>(most);
 }
 
-Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
+// weight_streaming: a plan of the swap-AB (weight-streaming) kind for every m <= 256, as the
+// fused quantisation needs (its CTAs quantise the token rows they read).
+Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count, bool weight_streaming = false) {
   Plan pl{};
   pl.ks = 1;
   pl.k_tiles = static_cast<int>(ceil_div(k, 256));
@@ -65,7 +67,14 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
   // the pairs (measured, cold PDL chains: 256 x 14336 x 4096 23.0 -> 16.0 us, 1024 x 4096 x 7168
   // 31.0 -> 23.8 us; with fewer tiles, e.g. 256 x 4096 x 7168, swap-AB split-K stays faster)
   const bool pair_tiles = n % 256 == 0 && m > 128 && ceil_div(m, 256) * (n / 256) >= sm_count / 4;
-  if (m <= 256 && !pair_tiles) {
+  // Short K (at most 8 K steps): 128 x 128 tiles over the whole K beat the swap-AB split-K plans
+  // from 17 tokens on, since the split's cluster reduction then costs more than the extra SMs
+  // streaming the weight gain (measured, PDL chains of 4 with cold weights, K = 2048: 32 / 64 /
+  // 128 / 256 x 7168 went 8.2 / 8.9 / 9.9 / 12.4 -> 7.8 / 7.8 / 8.2 / 8.8 us, 128 / 256 x 4096
+  // 9.6 / 12.4 -> 8.3 / 8.3, 128 x 14336 13.0 -> 9.0; at K = 4096 they lose where the tiles
+  // are few).  Kept to the measured N range.
+  const bool short_k = !weight_streaming && m > 16 && k <= 2048 && n >= 4096 && n <= 16384;
+  if (m <= 256 && (weight_streaming || (!pair_tiles && !short_k))) {
     pl.swap = 1;
     pl.bn = m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
     pl.m_tiles = static_cast<int>(ceil_div(n, 128));  // weight rows
@@ -103,7 +112,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count) {
       const int pairs = sm_count / 2;
       pl.dp_tiles = tiles;
       pl.ctas = 2 * (tiles < pairs ? tiles : pairs);
-    } else if (2 * tiles <= sm_count && units >= 4LL * sm_count) {
+    } else if (!short_k && 2 * tiles <= sm_count && units >= 4LL * sm_count) {
       // few tiles with a long K: whole tiles would leave most SMs idle
       pl.sk_tiles = tiles;
       pl.ctas = sm_count;
@@ -228,7 +237,7 @@ nvfp4_status_t run_gemm(const char *name, const uint8_t *a, const uint8_t *sfa, 
   nvfp4_status_t st = current_device(&dev);
   if (st != NVFP4_OK) return st;
 
-  const Plan pl = select_plan(m, n, k, dev.sm_count);
+  const Plan pl = select_plan(m, n, k, dev.sm_count, fused);
   // A swap-AB plan holds every token in one tile (tile_n >= m): the kernels read operand B's
   // scales with scale-factor ID 0, i.e. rows 0..BN-1 of each 128-row scale block, so a second
   // token tile at a row offset that is not a multiple of 128 would take the wrong scales.

@@ -74,6 +74,13 @@ def test_plan_selector_buckets(lib):
     # 16 pair tiles would fill too few: swap-AB, four-way cluster split-K
     assert lib.nvfp4_gemm_plan(256, 4096, 7168)["swap_ab"] == 1
     assert lib.nvfp4_gemm_plan(256, 14336, 4096)["tile_m"] == 256   # 56 pair tiles
+    # short K (8 steps) at N >= 4096: 128 x 128 tiles over the whole K instead of split-K
+    short = lib.nvfp4_gemm_plan(128, 7168, 2048)
+    assert short["swap_ab"] == 0 and short["tile_n"] == 128 and short["splits"] == 1
+    assert short["dp_tiles"] == 56 and short["sk_tiles"] == 0 and short["ctas"] == 56
+    assert lib.nvfp4_gemm_plan(256, 4096, 2048)["dp_tiles"] == 64
+    assert lib.nvfp4_gemm_plan(16, 7168, 2048)["swap_ab"] == 1     # up to 16 tokens: split-K
+    assert lib.nvfp4_gemm_plan(128, 7168, 4096)["swap_ab"] == 1    # longer K: split-K
     small = lib.nvfp4_gemm_plan(32, 1024, 1024)            # 8 tiles x 4 stages: one stage per CTA
     assert small["splits"] == 4 and small["ctas"] == 32
     few = lib.nvfp4_gemm_plan(640, 1024, 2048)             # 40 tiles but only 2 stages per SM

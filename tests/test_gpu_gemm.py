@@ -147,6 +147,18 @@ def test_prefill_sampled_rows(nv, m, n, k):
     assert_within(d[torch.from_numpy(rows).cuda()], R, tol, f"prefill {m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("m,n,k", [(17, 4096, 2048), (256, 4096, 1536)])
+def test_short_k_tiles_every_element(nv, m, n, k):
+    """Short K at N >= 4096 takes 128 x 128 tiles over the whole K rather than split-K from 17
+    tokens on; every element against the fp64 oracle (a ragged token tile, a K of 6 steps)."""
+    p = nv.nvfp4_gemm_plan(m, n, k)
+    assert p["swap_ab"] == 0 and p["splits"] == 1
+    ops = nvfp4_operands(m, n, k, 5)
+    d = _run(nv, ops)
+    R, tol = reference(ops)
+    assert_within(d, R, tol, f"short K {m}x{n}x{k}")
+
+
 def test_one_hot_probes(nv):
     """A single nonzero FP4 element of A (value 3, block scale 2) against an all-ones B with
     unit scales: exactly one output row is 6, the rest 0.  Sweeps nibble parity, block index
