@@ -144,7 +144,8 @@ nvfp4_status_t mxfp4_quantize(const void *x, int64_t t, int64_t k, int64_t ldx,
  * nvfp4_scaled_mm_kernels.cu "SM103 Dispatch"; narrow tiles for small M, [FI-4865]
  * "Reviewer Notes").  Up to 256 tokens the weight fills the MMA's 128-row slot and K is split
  * inside clusters, except where 256 x 256 CTA-pair tiles fill a quarter of the pairs, or where K
- * is at most 2048 (17 or more tokens, 4096 <= N <= 16384): there whole 128 x 128 tiles run.
+ * is short (4096 <= N <= 16384 and K <= 2048 from 17 tokens, K <= 4096 from 129): there whole
+ * 128 x 128 tiles run.
  * Host only. */
 typedef struct {
   int swap_ab;   /* 1: the weight B fills the 128-row MMA slot and tokens the N slot */

@@ -67,14 +67,19 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count, bool weight_stre
   // the pairs (measured, cold PDL chains: 256 x 14336 x 4096 23.0 -> 16.0 us, 1024 x 4096 x 7168
   // 31.0 -> 23.8 us; with fewer tiles, e.g. 256 x 4096 x 7168, swap-AB split-K stays faster)
   const bool pair_tiles = n % 256 == 0 && m > 128 && ceil_div(m, 256) * (n / 256) >= sm_count / 4;
-  // Short K (at most 8 K steps): 128 x 128 tiles over the whole K beat the swap-AB split-K plans
-  // from 17 tokens on, since the split's cluster reduction then costs more than the extra SMs
-  // streaming the weight gain (measured, PDL chains of 4 with cold weights, K = 2048: 32 / 64 /
-  // 128 / 256 x 7168 went 8.2 / 8.9 / 9.9 / 12.4 -> 7.8 / 7.8 / 8.2 / 8.8 us, 128 / 256 x 4096
-  // 9.6 / 12.4 -> 8.3 / 8.3, 128 x 14336 13.0 -> 9.0; at K = 4096 they lose where the tiles
-  // are few).  Kept to the measured N range.
-  const bool short_k = !weight_streaming && m > 16 && k <= 2048 && n >= 4096 && n <= 16384;
-  if (m <= 256 && (weight_streaming || (!pair_tiles && !short_k))) {
+  // Whole 128 x 128 tiles beat the swap-AB split-K plans where K is short, since the split's
+  // cluster reduction then costs more than the extra SMs streaming the weight gain (measured,
+  // PDL chains of cold weights, us per GEMM):
+  //  - K <= 2048 from 17 tokens on: 32 / 64 / 128 / 256 x 7168 x 2048 8.2 / 8.9 / 9.9 / 12.4 ->
+  //    7.8 / 7.8 / 8.2 / 8.8, 128 / 256 x 4096 x 2048 9.6 / 12.4 -> 8.3 / 8.3, 128 x 14336 x 2048
+  //    13.0 -> 9.0;
+  //  - K <= 4096 from 129 tokens on (two token tiles): 256 x 7168 x 4096 15.0 -> 12.0, 256 x 4096
+  //    x 4096 13.6 -> 11.6.  With one token tile (128 x 4096 x 4096: 10.9 -> 11.5) or at K = 7168
+  //    with 64 tiles (256 x 4096 x 7168: 14.3 -> 15.7) they lose.
+  // Kept to the measured N range, and never split stream-K (which measured slower here).
+  const bool whole_tiles = !weight_streaming && n >= 4096 && n <= 16384 &&
+                           ((m > 16 && k <= 2048) || (m > 128 && k <= 4096));
+  if (m <= 256 && (weight_streaming || (!pair_tiles && !whole_tiles))) {
     pl.swap = 1;
     pl.bn = m <= 32 ? 32 : m <= 64 ? 64 : m <= 128 ? 128 : 256;
     pl.m_tiles = static_cast<int>(ceil_div(n, 128));  // weight rows
@@ -112,7 +117,7 @@ Plan select_plan(int64_t m, int64_t n, int64_t k, int sm_count, bool weight_stre
       const int pairs = sm_count / 2;
       pl.dp_tiles = tiles;
       pl.ctas = 2 * (tiles < pairs ? tiles : pairs);
-    } else if (!short_k && 2 * tiles <= sm_count && units >= 4LL * sm_count) {
+    } else if (!whole_tiles && 2 * tiles <= sm_count && units >= 4LL * sm_count) {
       // few tiles with a long K: whole tiles would leave most SMs idle
       pl.sk_tiles = tiles;
       pl.ctas = sm_count;

@@ -80,7 +80,10 @@ def test_plan_selector_buckets(lib):
     assert short["dp_tiles"] == 56 and short["sk_tiles"] == 0 and short["ctas"] == 56
     assert lib.nvfp4_gemm_plan(256, 4096, 2048)["dp_tiles"] == 64
     assert lib.nvfp4_gemm_plan(16, 7168, 2048)["swap_ab"] == 1     # up to 16 tokens: split-K
-    assert lib.nvfp4_gemm_plan(128, 7168, 4096)["swap_ab"] == 1    # longer K: split-K
+    assert lib.nvfp4_gemm_plan(128, 7168, 4096)["swap_ab"] == 1    # longer K, one token tile: split-K
+    two = lib.nvfp4_gemm_plan(256, 7168, 4096)                      # two token tiles, K <= 4096
+    assert two["swap_ab"] == 0 and two["dp_tiles"] == 112 and two["sk_tiles"] == 0 and two["ctas"] == 112
+    assert lib.nvfp4_gemm_plan(256, 4096, 7168)["swap_ab"] == 1    # K = 7168: split-K
     small = lib.nvfp4_gemm_plan(32, 1024, 1024)            # 8 tiles x 4 stages: one stage per CTA
     assert small["splits"] == 4 and small["ctas"] == 32
     few = lib.nvfp4_gemm_plan(640, 1024, 2048)             # 40 tiles but only 2 stages per SM

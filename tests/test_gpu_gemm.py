@@ -147,10 +147,11 @@ def test_prefill_sampled_rows(nv, m, n, k):
     assert_within(d[torch.from_numpy(rows).cuda()], R, tol, f"prefill {m}x{n}x{k}")
 
 
-@pytest.mark.parametrize("m,n,k", [(17, 4096, 2048), (256, 4096, 1536)])
+@pytest.mark.parametrize("m,n,k", [(17, 4096, 2048), (256, 4096, 1536), (200, 7168, 4096)])
 def test_short_k_tiles_every_element(nv, m, n, k):
-    """Short K at N >= 4096 takes 128 x 128 tiles over the whole K rather than split-K from 17
-    tokens on; every element against the fp64 oracle (a ragged token tile, a K of 6 steps)."""
+    """Short K at N >= 4096 takes 128 x 128 tiles over the whole K rather than split-K (from 17
+    tokens on at K <= 2048, from 129 at K <= 4096); every element against the fp64 oracle (ragged
+    token tiles, a K of 6 steps)."""
     p = nv.nvfp4_gemm_plan(m, n, k)
     assert p["swap_ab"] == 0 and p["splits"] == 1
     ops = nvfp4_operands(m, n, k, 5)
