@@ -1,10 +1,11 @@
 // The MoE steps around the grouped GEMMs, NVFP4 flavour: expert sort of the routed tokens,
-// row gather, per-expert NVFP4 quantisation (plain, or fused with SiLU-and-mul), weighted
-// combine.  Named on vLLM fork compare view "add pdl" (ops.h, torch_bindings.cpp:
+// row gather, per-expert NVFP4 quantisation (plain, fused with the row gather, or fused with
+// SiLU-and-mul), weighted combine.  Named on vLLM fork compare view "add pdl" (ops.h, torch_bindings.cpp:
 // scaled_fp4_experts_quant, silu_and_mul_scaled_fp4_experts_quant with input_offset_by_experts /
 // output_scale_offset_by_experts) and vLLM PR 51158 "Changes" (experts quantise, grouped GEMM);
 // the pages give names and arguments only, the definitions used are stated per entry point in
-// nvfp4.h.  All of these are bandwidth-bound CUDA-core kernels.
+// nvfp4.h.  All of these are CUDA-core kernels: the gather and combine are bound by memory
+// bandwidth, the sort by latency, and the per-expert quantisers by instruction issue.
 #include <cuda_bf16.h>
 
 #include "host.h"
