@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kPlaceWarps * 32) moe_place_kernel(const int32
 // ------------------------------------------------------------------ row gather
 // out[r, :] = x[src[r], :] for r < rows; 16-byte pieces, grid-stride.  A source row outside
 // [0, T) sets bit 3 of the status word and its output row is left untouched.
-// I: the position type (32-bit when rows * pieces < 2^31: a cheaper division per position).
+// I: the position type (32-bit when rows * pieces plus one grid stride < 2^31: a cheaper
+// division per position).
 template <typename I>
 __global__ void __launch_bounds__(256) moe_gather_kernel(const uint4 *__restrict__ x, int64_t ldx16, int64_t T,
                                                          const int32_t *__restrict__ src, int64_t rows,

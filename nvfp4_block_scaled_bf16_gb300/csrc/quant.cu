@@ -49,7 +49,8 @@ __device__ __forceinline__ uint32_t gather4(uint32_t code) {
 
 // total = round_up(m,128) * cp, a multiple of 512, so every warp runs the same trip count.
 // SM103: scales in the SM103 layout instead of the 128x4 one.  I: the position type (32-bit
-// when total < 2^31: its division is several times cheaper than the 64-bit one).
+// when total plus one grid stride < 2^31: its division is several times cheaper than the
+// 64-bit one).
 template <bool SM103, typename I>
 __global__ void __launch_bounds__(256) nvfp4_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                           int64_t m, int64_t kb, int64_t ldx,
