@@ -110,6 +110,39 @@ def test_swap_plans_hold_every_token_in_one_tile(lib):
                 assert p["tile_n"] >= m, (m, n, k, p)
 
 
+def test_plan_invariants_over_a_shape_sweep(lib):
+    """Every plan the selector makes (152 SMs without a device) is launchable and covers the
+    output exactly once: swap-AB plans hold all tokens in one tile and split K at most 8 ways
+    over one CTA per split; other plans never split inside a cluster; whole plus stream-K tiles
+    are the output tiles; a workspace is needed exactly when tiles are split stream-K; short-K
+    whole-tile plans never fall back to stream-K."""
+    ms = [1, 2, 16, 17, 31, 32, 33, 64, 65, 100, 128, 129, 200, 256, 257, 300, 512, 1024, 2048, 4096, 6000]
+    ns = [256, 512, 1024, 2048, 4096, 7168, 8192, 13056, 14336, 16384, 19456, 28672]
+    ks = [256, 512, 768, 1536, 2048, 2304, 4096, 7168, 16384]
+    for m in ms:
+        for n in ns:
+            for k in ks:
+                p = lib.nvfp4_gemm_plan(m, n, k)
+                ws = lib.gemm_workspace_size(m, n, k)
+                where = (m, n, k, p)
+                assert p["ctas"] >= 1 and p["stages"] >= 2 and p["tile_n"] in (32, 64, 128, 256), where
+                k_steps = -(-k // 256)
+                if p["swap_ab"]:
+                    assert m <= 256 and p["tile_n"] >= m and p["tile_m"] == 128, where
+                    assert 1 <= p["splits"] <= min(8, k_steps), where
+                    assert p["dp_tiles"] == -(-n // 128) and p["sk_tiles"] == 0, where
+                    assert p["ctas"] == p["dp_tiles"] * p["splits"] and ws == 0, where
+                else:
+                    assert p["splits"] == 1, where
+                    tiles = -(-m // p["tile_m"]) * -(-n // p["tile_n"])
+                    assert p["dp_tiles"] + p["sk_tiles"] == tiles, where
+                    assert (ws > 0) == (p["sk_tiles"] > 0), where
+                    if p["tile_m"] == 256:
+                        assert p["tile_n"] == 256 and p["ctas"] % 2 == 0 and p["sk_tiles"] == 0, where
+                    if m <= 256 and p["tile_m"] == 128:   # a short-K whole-tile plan
+                        assert p["sk_tiles"] == 0 and p["ctas"] == min(tiles, 152), where
+
+
 def test_workspace_size(lib):
     """Counters (one per split tile, padded to 256 B) + 2 fp32 slots of 128 x tile_n per CTA."""
     assert lib.gemm_workspace_size(1, 4096, 7168) == 0        # cluster split-K needs none
